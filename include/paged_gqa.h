@@ -1,0 +1,174 @@
+/*
+ * paged_gqa.h -- C ABI of the GB300 (sm_103a) paged grouped-query attention library.
+ *
+ * One call computes, for a varlen batch of sequences, attention of the new query
+ * tokens over a paged (block-tabled) KV cache with head_dim 256:
+ *
+ *   for each sequence s (q0 = query_start_loc[s], qn = query_start_loc[s+1] - q0,
+ *   L = seq_lens[s]), query token t < qn and query head h:
+ *     kvh = h / (Hq / Hkv)                         contiguous GQA head groups
+ *     keys j = 0 .. L - qn + t                     bottom-right causal mask
+ *     K_j  = k_cache[block_table[s, j / P], j % P, kvh, :] * k_descale
+ *     V_j  = v_cache[block_table[s, j / P], j % P, kvh, :] * v_descale
+ *     out[q0 + t, h, :] = softmax_j(softmax_scale * q . K_j) . V_j      (bf16)
+ *
+ * Where each piece comes from:
+ *   - paged K/V with separate K and V views, one kv-head grid dimension, per-tensor
+ *     FP8 descale scalars, query heads grouped per kv head:
+ *     "Optimize Qwen3.5 MTP unified attention on gfx950" (sglang #36330), review
+ *     thread on kv-head-generic launch and the Modifications section;
+ *   - new tokens attending to cached + new K/V (cu_seqlens_k longer than
+ *     cu_seqlens_q) under a bottom-right causal mask:
+ *     "asm FP8 FMHA for prefix-hit prefill" (ROCm/ATOM #2534), summary;
+ *   - a block table whose row stride is a runtime value and 64-token pages:
+ *     "gfx1250 GDN prefill kernels ...; DP points on unified attention"
+ *     (ROCm/ATOM #2830), description and commit 6.
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer inside a pg_tensor is a DEVICE pointer on the current CUDA
+ *     device. Shapes and strides are in elements. The innermost dimension of q,
+ *     the caches and out must be contiguous (stride 1).
+ *   - The caller owns every tensor. Calls are asynchronous and ordered on
+ *     `stream`; the library keeps no pointer to caller memory once the call's
+ *     work on `stream` has completed.
+ *   - seq_lens[s] is the TOTAL K/V length of sequence s, new tokens included
+ *     (their K/V must already be in the cache). 0 <= qn <= L <= W * P.
+ *   - Block-table entries past ceil(L / P) are never read and may hold anything.
+ *   - Cache slots at positions >= L are never read into the result: their
+ *     contents (NaN included) do not change the output.
+ *   - Return value: PG_OK (0) or a negative pg_status. A host-side error launches
+ *     nothing; the message is available from paged_gqa_last_error().
+ *   - Violations only visible on the device (qn > L, L > W * P, a block-table
+ *     entry outside [0, NB)) never trap: the kernels record a code in a device
+ *     error word, write zeros to the affected rows, and go on.
+ *     paged_gqa_check_device_errors() reports and clears it.
+ */
+#ifndef PAGED_GQA_H_
+#define PAGED_GQA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* pg_stream_t;
+
+typedef enum {
+  PG_BF16 = 1,
+  PG_F16 = 2,   /* accepted by no entry point today; reserved */
+  PG_E4M3 = 3,  /* OCP FP8 e4m3fn (max 448, no inf, 0x7F/0xFF are NaN) */
+  PG_I32 = 4,
+  PG_F32 = 5
+} pg_dtype;
+
+/* A strided view. Unused trailing shape/stride entries are ignored. */
+typedef struct {
+  void* data;
+  int32_t dtype;      /* pg_dtype */
+  int32_t ndim;
+  int64_t shape[4];
+  int64_t stride[4];  /* elements */
+} pg_tensor;
+
+typedef enum {
+  PG_OK = 0,
+  PG_ERR_INVALID_ARG = -1,   /* null pointer, shape/stride mismatch, Hq % Hkv != 0,
+                                misaligned base or row stride, non-contiguous last dim */
+  PG_ERR_UNSUPPORTED = -2,   /* head_dim != 256, out not bf16, FP8 q with bf16 K/V,
+                                page size not in {16, 32, 64, 128} */
+  PG_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed */
+  PG_ERR_TIMEOUT = -4,       /* device: a bounded wait gave up (reported by
+                                paged_gqa_check_device_errors) */
+  PG_ERR_DEVICE_BOUNDS = -5, /* device: qn > L, L > W*P or a page id outside [0, NB) */
+  PG_ERR_WORKSPACE = -6      /* caller workspace too small or misaligned */
+} pg_status;
+
+/*
+ * paged_gqa_attn -- the call.
+ *
+ *   q               [T, Hq, 256]        bf16, or e4m3 (then K/V must be e4m3;
+ *                                        fold q's descale into softmax_scale)
+ *   k_cache         [NB, P, Hkv, 256]   bf16 or e4m3; any strides on dims 0..2 that
+ *                                        are multiples of 16 bytes; base 16-byte aligned
+ *   v_cache         same shape and dtype as k_cache (its own strides)
+ *   block_table     [num_seqs, W]       int32, physical page ids; any row stride
+ *   seq_lens        [num_seqs]          int32, total K/V length per sequence
+ *   query_start_loc [num_seqs + 1]      int32, [0] == 0, non-decreasing, [num_seqs] == T
+ *   k_descale, v_descale                per-tensor dequant scales (pass 1 for bf16)
+ *   softmax_scale                       multiplies q . k (usually 1/16 for hd 256)
+ *   out             [T, Hq, 256]        bf16, written for every (token, head)
+ *   stream                              CUDA stream the work is ordered on
+ *
+ * Uses a library-owned workspace per device that grows on first need
+ * (cudaMalloc: do not call this inside CUDA-graph capture on a new shape; use
+ * paged_gqa_attn_ex with your own workspace there).
+ */
+int paged_gqa_attn(const pg_tensor* q, const pg_tensor* k_cache, const pg_tensor* v_cache,
+                   const pg_tensor* block_table, const pg_tensor* seq_lens,
+                   const pg_tensor* query_start_loc, float k_descale, float v_descale,
+                   float softmax_scale, pg_tensor* out, pg_stream_t stream);
+
+/*
+ * paged_gqa_attn_ex -- the same call with an explicit q descale (multiplied into
+ * softmax_scale) and a caller-owned device workspace of at least
+ * paged_gqa_workspace_size(...) bytes, 256-byte aligned. Allocates nothing.
+ * The workspace must not be shared by calls that can overlap on the device.
+ */
+int paged_gqa_attn_ex(const pg_tensor* q, const pg_tensor* k_cache, const pg_tensor* v_cache,
+                      const pg_tensor* block_table, const pg_tensor* seq_lens,
+                      const pg_tensor* query_start_loc, float q_descale, float k_descale,
+                      float v_descale, float softmax_scale, pg_tensor* out,
+                      void* workspace, size_t workspace_bytes, pg_stream_t stream);
+
+/*
+ * Workspace bytes for a call with these host-known sizes on `device`
+ * (num_seqs, total query tokens T, heads, page size, block-table width W).
+ * Returns 0 on invalid sizes.
+ */
+size_t paged_gqa_workspace_size(int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
+                                int page_size, int max_blocks_per_seq, int device);
+
+/* Message of the last non-zero status returned on this host thread ("" if none). */
+const char* paged_gqa_last_error(void);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's error word.
+ * Returns PG_OK, PG_ERR_DEVICE_BOUNDS, PG_ERR_TIMEOUT or PG_ERR_CUDA.
+ */
+int paged_gqa_check_device_errors(pg_stream_t stream);
+
+/*
+ * Kernel path selection, for tests and sweeps (process-wide):
+ *   0 = automatic (tcgen05 kernels where they apply, warp-level MMA otherwise)
+ *   1 = warp-level MMA (mma.sync) kernel for every tile
+ * Returns the previous value, or PG_ERR_INVALID_ARG.
+ */
+int paged_gqa_set_path(int path);
+
+/*
+ * Host-side launch summary of the last successful call on this host thread, for
+ * tests and the benchmark. out8 receives {verify CTAs, prefill CTAs, kernels
+ * launched, path bits (2: tcgen05 verify, 4: tcgen05 prefill, 8: warp-MMA verify,
+ * 16: warp-MMA prefill), verify block bound, prefill block bound, workspace bytes, 0}.
+ */
+int paged_gqa_last_plan(int64_t* out8);
+
+/*
+ * Profiling hook (process-wide): while set, every call records `start` on its stream
+ * immediately before the attention kernel of class `cls` (0 = verify blocks,
+ * 1 = prefill blocks) and `stop` immediately after it. Both are cudaEvent_t handles
+ * owned by the caller; pass NULLs to stop recording. Returns PG_OK or
+ * PG_ERR_INVALID_ARG.
+ */
+int paged_gqa_set_kernel_events(int cls, void* start, void* stop);
+
+/* Library ABI version (major * 100 + minor). */
+int paged_gqa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGED_GQA_H_ */

@@ -1,0 +1,179 @@
+"""ctypes binding of libpaged_gqa.so: argument marshalling only."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+PG_BF16, PG_F16, PG_E4M3, PG_I32, PG_F32 = 1, 2, 3, 4, 5
+STATUS_NAMES = {0: "PG_OK", -1: "PG_ERR_INVALID_ARG", -2: "PG_ERR_UNSUPPORTED", -3: "PG_ERR_CUDA",
+                -4: "PG_ERR_TIMEOUT", -5: "PG_ERR_DEVICE_BOUNDS", -6: "PG_ERR_WORKSPACE"}
+
+# Every symbol include/paged_gqa.h declares.
+EXPORTED = ("paged_gqa_attn", "paged_gqa_attn_ex", "paged_gqa_workspace_size", "paged_gqa_last_error",
+            "paged_gqa_check_device_errors", "paged_gqa_set_path", "paged_gqa_last_plan",
+            "paged_gqa_set_kernel_events", "paged_gqa_version")
+
+
+class PagedGQAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class PgTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load the library (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if build_if_missing:
+                _build.build()
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError(f"libpaged_gqa.so not found at {_build.LIB}; run paged_gqa_gb300.build")
+            lib = ctypes.CDLL(_build.LIB)
+            P = ctypes.POINTER(PgTensor)
+            f, c_vp = ctypes.c_float, ctypes.c_void_p
+            lib.paged_gqa_attn.argtypes = [P, P, P, P, P, P, f, f, f, P, c_vp]
+            lib.paged_gqa_attn.restype = ctypes.c_int
+            lib.paged_gqa_attn_ex.argtypes = [P, P, P, P, P, P, f, f, f, f, P, c_vp, ctypes.c_size_t, c_vp]
+            lib.paged_gqa_attn_ex.restype = ctypes.c_int
+            lib.paged_gqa_workspace_size.argtypes = [ctypes.c_int] * 7
+            lib.paged_gqa_workspace_size.restype = ctypes.c_size_t
+            lib.paged_gqa_last_error.restype = ctypes.c_char_p
+            lib.paged_gqa_check_device_errors.argtypes = [c_vp]
+            lib.paged_gqa_check_device_errors.restype = ctypes.c_int
+            lib.paged_gqa_set_path.argtypes = [ctypes.c_int]
+            lib.paged_gqa_set_path.restype = ctypes.c_int
+            lib.paged_gqa_last_plan.argtypes = [ctypes.POINTER(ctypes.c_int64)]
+            lib.paged_gqa_last_plan.restype = ctypes.c_int
+            lib.paged_gqa_version.restype = ctypes.c_int
+            lib.paged_gqa_set_kernel_events.argtypes = [ctypes.c_int, c_vp, c_vp]
+            lib.paged_gqa_set_kernel_events.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def exported_symbols():
+    lib = load()
+    return {name: hasattr(lib, name) for name in EXPORTED}
+
+
+_DTYPES = {torch.bfloat16: PG_BF16, torch.float16: PG_F16, torch.int32: PG_I32, torch.float32: PG_F32,
+           torch.uint8: PG_E4M3}
+if hasattr(torch, "float8_e4m3fn"):
+    _DTYPES[torch.float8_e4m3fn] = PG_E4M3
+
+
+def _desc(t: Optional[torch.Tensor], dtype: Optional[int] = None) -> PgTensor:
+    """pg_tensor view of a torch tensor (uint8 is read as e4m3 bit patterns)."""
+    d = PgTensor()
+    if t is None:
+        return d
+    if t.dim() > 4:
+        raise ValueError("at most 4 dims")
+    d.data = t.data_ptr() if t.numel() > 0 else 0
+    d.dtype = dtype if dtype is not None else _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status: int):
+    if status != 0:
+        msg = load().paged_gqa_last_error().decode(errors="replace")
+        raise PagedGQAError(status, msg)
+
+
+def paged_gqa_attn(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, k_descale: float,
+                   v_descale: float, softmax_scale: float, out, stream=None) -> None:
+    """out[T, Hq, 256] (bf16) = paged GQA attention; see include/paged_gqa.h."""
+    lib = load()
+    a = [_desc(q), _desc(k_cache), _desc(v_cache), _desc(block_table), _desc(seq_lens),
+         _desc(query_start_loc)]
+    o = _desc(out)
+    _check(lib.paged_gqa_attn(*[ctypes.byref(x) for x in a], float(k_descale), float(v_descale),
+                              float(softmax_scale), ctypes.byref(o), _stream(stream)))
+
+
+def paged_gqa_attn_ex(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, q_descale: float,
+                      k_descale: float, v_descale: float, softmax_scale: float, out, workspace,
+                      stream=None) -> None:
+    """Same as paged_gqa_attn with q_descale and a caller-owned workspace tensor."""
+    lib = load()
+    a = [_desc(q), _desc(k_cache), _desc(v_cache), _desc(block_table), _desc(seq_lens),
+         _desc(query_start_loc)]
+    o = _desc(out)
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    ptr = workspace.data_ptr() if workspace is not None else None
+    _check(lib.paged_gqa_attn_ex(*[ctypes.byref(x) for x in a], float(q_descale), float(k_descale),
+                                 float(v_descale), float(softmax_scale), ctypes.byref(o), ptr, nbytes,
+                                 _stream(stream)))
+
+
+def paged_gqa_workspace_size(num_seqs: int, total_q: int, num_q_heads: int, num_kv_heads: int,
+                             page_size: int, max_blocks_per_seq: int, device: int = 0) -> int:
+    return int(load().paged_gqa_workspace_size(num_seqs, total_q, num_q_heads, num_kv_heads, page_size,
+                                               max_blocks_per_seq, device))
+
+
+def paged_gqa_last_error() -> str:
+    return load().paged_gqa_last_error().decode(errors="replace")
+
+
+def paged_gqa_check_device_errors(stream=None) -> int:
+    """Synchronise, read and clear the device error word; returns the status code."""
+    return int(load().paged_gqa_check_device_errors(_stream(stream)))
+
+
+def paged_gqa_set_path(path: int) -> int:
+    r = int(load().paged_gqa_set_path(path))
+    if r < 0:
+        _check(r)
+    return r
+
+
+def paged_gqa_last_plan() -> dict:
+    buf = (ctypes.c_int64 * 8)()
+    _check(load().paged_gqa_last_plan(buf))
+    keys = ("verify_ctas", "prefill_ctas", "kernels_launched", "path_bits", "max_verify_blocks",
+            "max_prefill_blocks", "workspace_bytes", "reserved")
+    return dict(zip(keys, list(buf)))
+
+
+def paged_gqa_set_kernel_events(cls: int, start=None, stop=None) -> None:
+    """Record torch.cuda.Event pairs around the class-`cls` attention kernel (None clears)."""
+    h0 = start.cuda_event if start is not None else None
+    h1 = stop.cuda_event if stop is not None else None
+    _check(load().paged_gqa_set_kernel_events(int(cls), h0, h1))
+
+
+def paged_gqa_version() -> int:
+    return int(load().paged_gqa_version())

@@ -1,0 +1,429 @@
+// api.cu -- host side of the C ABI declared in include/paged_gqa.h.
+//
+// Validates the descriptors, sizes the workspace from host-known bounds, and issues
+// the launches on the caller's stream: the plan kernel, then one persistent attention
+// kernel per class of row blocks (verify: q_len*G <= 64 rows; prefill: 128-row blocks).
+// Nothing here reads device memory, so a call never synchronises.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/paged_gqa.h"
+#include "common.cuh"
+#include "plan.cuh"
+#include "tc_kernels.cuh"
+
+namespace pgqa {
+__device__ uint32_t g_error_word;
+}
+
+using namespace pgqa;
+
+namespace {
+
+thread_local std::string t_last_error;
+thread_local int64_t t_last_plan[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+std::atomic<int> g_path{0};
+std::atomic<cudaEvent_t> g_ev_start[kNumClasses], g_ev_stop[kNumClasses];
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PG_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::mutex mu;
+  int sms = 0;
+  uint32_t* err = nullptr;   // address of g_error_word on this device
+  void* ws = nullptr;        // library-owned workspace
+  size_t ws_bytes = 0;
+};
+DeviceState g_dev[kMaxDevices];
+
+int device_state(int dev, DeviceState** out) {
+  if (dev < 0 || dev >= kMaxDevices) return fail(PG_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  DeviceState& s = g_dev[dev];
+  std::lock_guard<std::mutex> lk(s.mu);
+  if (s.sms == 0) {
+    int sms = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    void* addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_error_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    s.err = static_cast<uint32_t*>(addr);
+    s.sms = sms;
+  }
+  *out = &s;
+  return PG_OK;
+}
+
+// ---------------------------------------------------------------- workspace layout --
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct ClassSizes {
+  int num_ctas, max_blocks, max_items, max_slots;
+};
+
+struct WsLayout {
+  ClassSizes cls[kNumClasses];
+  size_t off[kNumClasses][8];
+  size_t total;
+};
+
+WsLayout make_layout(int num_seqs, int T, int Hq, int Hkv, int sms) {
+  WsLayout L{};
+  const long long G = Hq / Hkv;
+  const long long rows_all = (long long)T * G;
+  // verify blocks: one per (sequence, kv head); prefill blocks: 128-row blocks
+  const long long vb = (long long)num_seqs * Hkv;
+  const long long pb = (long long)Hkv * ((rows_all + kPrefillRows - 1) / kPrefillRows + num_seqs);
+  const long long nb[2] = {vb, pb};
+  size_t at = 0;
+  for (int c = 0; c < kNumClasses; ++c) {
+    ClassSizes& s = L.cls[c];
+    s.num_ctas = sms;
+    s.max_blocks = (int)std::max<long long>(1, nb[c]);
+    s.max_items = s.max_blocks + s.num_ctas;
+    s.max_slots = 2 * s.num_ctas;
+    size_t sz[8] = {
+        256,                                                        // n_blocks, n_items, total_tiles
+        sizeof(int) * (size_t)(s.num_ctas + 1),                     // cta_item_begin
+        sizeof(RowBlock) * (size_t)s.max_blocks,                    // blocks
+        sizeof(WorkItem) * (size_t)s.max_items,                     // items
+        sizeof(int) * (size_t)s.max_blocks,                         // counters
+        sizeof(float) * (size_t)s.max_slots * kSlotRows * kHeadDim, // part_o
+        sizeof(float) * (size_t)s.max_slots * kSlotRows,            // part_lse
+        0};
+    for (int i = 0; i < 8; ++i) {
+      L.off[c][i] = at;
+      at += align256(sz[i]);
+    }
+  }
+  L.total = at;
+  return L;
+}
+
+ClassPlan class_plan(const WsLayout& L, int c, char* base) {
+  ClassPlan cp{};
+  const size_t* o = L.off[c];
+  cp.n_blocks = reinterpret_cast<int*>(base + o[0]);
+  cp.n_items = reinterpret_cast<int*>(base + o[0] + 8);
+  cp.total_tiles = reinterpret_cast<long long*>(base + o[0] + 16);
+  cp.cta_item_begin = reinterpret_cast<int*>(base + o[1]);
+  cp.blocks = reinterpret_cast<RowBlock*>(base + o[2]);
+  cp.items = reinterpret_cast<WorkItem*>(base + o[3]);
+  cp.counters = reinterpret_cast<int*>(base + o[4]);
+  cp.part_o = reinterpret_cast<float*>(base + o[5]);
+  cp.part_lse = reinterpret_cast<float*>(base + o[6]);
+  cp.num_ctas = L.cls[c].num_ctas;
+  cp.max_blocks = L.cls[c].max_blocks;
+  cp.max_items = L.cls[c].max_items;
+  cp.max_slots = L.cls[c].max_slots;
+  return cp;
+}
+
+// ---------------------------------------------------------------- validation --
+
+struct Validated {
+  Problem p;
+  Pointers ptr;
+};
+
+int check_tensor(const pg_tensor* t, const char* name, int ndim) {
+  if (!t) return fail(PG_ERR_INVALID_ARG, "%s: null descriptor", name);
+  if (t->ndim != ndim) return fail(PG_ERR_INVALID_ARG, "%s: expected %d dims, got %d", name, ndim, t->ndim);
+  for (int i = 0; i < ndim; ++i)
+    if (t->shape[i] < 0) return fail(PG_ERR_INVALID_ARG, "%s: negative extent", name);
+  return PG_OK;
+}
+
+int validate(const pg_tensor* q, const pg_tensor* k, const pg_tensor* v, const pg_tensor* bt,
+             const pg_tensor* sl, const pg_tensor* qsl, float q_descale, float k_descale,
+             float v_descale, float softmax_scale, const pg_tensor* out, Validated* res) {
+  int st;
+  if ((st = check_tensor(q, "q", 3)) || (st = check_tensor(k, "k_cache", 4)) ||
+      (st = check_tensor(v, "v_cache", 4)) || (st = check_tensor(bt, "block_table", 2)) ||
+      (st = check_tensor(sl, "seq_lens", 1)) || (st = check_tensor(qsl, "query_start_loc", 1)) ||
+      (st = check_tensor(out, "out", 3)))
+    return st;
+  if (q->shape[2] != kHeadDim || k->shape[3] != kHeadDim)
+    return fail(PG_ERR_UNSUPPORTED, "head_dim must be 256 (q %lld, cache %lld)", (long long)q->shape[2],
+                (long long)k->shape[3]);
+  if (q->dtype != PG_BF16 && q->dtype != PG_E4M3) return fail(PG_ERR_UNSUPPORTED, "q dtype must be bf16 or e4m3");
+  if (k->dtype != PG_BF16 && k->dtype != PG_E4M3) return fail(PG_ERR_UNSUPPORTED, "cache dtype must be bf16 or e4m3");
+  if (v->dtype != k->dtype) return fail(PG_ERR_INVALID_ARG, "k_cache and v_cache dtypes differ");
+  if (q->dtype == PG_E4M3 && k->dtype != PG_E4M3)
+    return fail(PG_ERR_UNSUPPORTED, "e4m3 q needs an e4m3 cache");
+  if (out->dtype != PG_BF16) return fail(PG_ERR_UNSUPPORTED, "out must be bf16");
+  if (bt->dtype != PG_I32 || sl->dtype != PG_I32 || qsl->dtype != PG_I32)
+    return fail(PG_ERR_INVALID_ARG, "block_table, seq_lens and query_start_loc must be int32");
+  for (int i = 0; i < 4; ++i)
+    if (k->shape[i] != v->shape[i]) return fail(PG_ERR_INVALID_ARG, "k_cache and v_cache shapes differ");
+  const long long T = q->shape[0], Hq = q->shape[1];
+  const long long NB = k->shape[0], P = k->shape[1], Hkv = k->shape[2];
+  const long long S = sl->shape[0], W = bt->shape[1];
+  if (out->shape[0] != T || out->shape[1] != Hq || out->shape[2] != kHeadDim)
+    return fail(PG_ERR_INVALID_ARG, "out shape must equal q shape");
+  if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0)
+    return fail(PG_ERR_INVALID_ARG, "num_q_heads (%lld) must be a positive multiple of num_kv_heads (%lld)", Hq, Hkv);
+  if (P != 16 && P != 32 && P != 64 && P != 128)
+    return fail(PG_ERR_UNSUPPORTED, "page size %lld not in {16, 32, 64, 128}", P);
+  if (bt->shape[0] != S || qsl->shape[0] != S + 1)
+    return fail(PG_ERR_INVALID_ARG, "block_table rows / query_start_loc length must match seq_lens");
+  if (T > INT32_MAX / 2 || NB > INT32_MAX || S > INT32_MAX / 2 || W > INT32_MAX / 2 || Hq > 65535)
+    return fail(PG_ERR_UNSUPPORTED, "sizes beyond the supported range");
+  if (q->stride[2] != 1 || k->stride[3] != 1 || v->stride[3] != 1 || out->stride[2] != 1)
+    return fail(PG_ERR_INVALID_ARG, "the head_dim axis must be contiguous");
+  if (W > 1 && bt->stride[1] != 1) return fail(PG_ERR_INVALID_ARG, "block_table rows must be contiguous");
+  if ((S > 0 && sl->stride[0] != 1) || qsl->stride[0] != 1)
+    return fail(PG_ERR_INVALID_ARG, "seq_lens and query_start_loc must be contiguous");
+  const int qesz = q->dtype == PG_E4M3 ? 1 : 2, kesz = k->dtype == PG_E4M3 ? 1 : 2;
+  if (!aligned16(q->data) || !aligned16(k->data) || !aligned16(v->data) || !aligned16(out->data))
+    return fail(PG_ERR_INVALID_ARG, "q, caches and out must be 16-byte aligned");
+  for (int i = 0; i < 2; ++i)
+    if ((q->stride[i] * qesz) % 16 || (out->stride[i] * 2) % 16)
+      return fail(PG_ERR_INVALID_ARG, "q/out strides must be multiples of 16 bytes");
+  for (int i = 0; i < 3; ++i)
+    if ((k->stride[i] * kesz) % 16 || (v->stride[i] * kesz) % 16)
+      return fail(PG_ERR_INVALID_ARG, "cache strides must be multiples of 16 bytes");
+  if ((T > 0 && (!q->data || !out->data)) || (NB > 0 && (!k->data || !v->data)) || !qsl->data ||
+      (S > 0 && (!sl->data || (W > 0 && !bt->data))))
+    return fail(PG_ERR_INVALID_ARG, "null data pointer");
+  if (!std::isfinite(softmax_scale) || !std::isfinite(k_descale) || !std::isfinite(v_descale) ||
+      !std::isfinite(q_descale))
+    return fail(PG_ERR_INVALID_ARG, "scales must be finite");
+
+  Problem& p = res->p;
+  p.num_seqs = (int)S;
+  p.T = (int)T;
+  p.Hq = (int)Hq;
+  p.Hkv = (int)Hkv;
+  p.G = (int)(Hq / Hkv);
+  p.P = (int)P;
+  p.W = (int)W;
+  p.NB = (int)NB;
+  p.q_is_fp8 = q->dtype == PG_E4M3;
+  p.kv_is_fp8 = k->dtype == PG_E4M3;
+  p.q_st = q->stride[0];
+  p.q_sh = q->stride[1];
+  p.k_sb = k->stride[0];
+  p.k_sp = k->stride[1];
+  p.k_sh = k->stride[2];
+  p.v_sb = v->stride[0];
+  p.v_sp = v->stride[1];
+  p.v_sh = v->stride[2];
+  p.o_st = out->stride[0];
+  p.o_sh = out->stride[1];
+  p.bt_stride = W > 0 ? bt->stride[0] : 1;
+  p.score_scale_log2 = (float)((double)softmax_scale * (double)q_descale * (double)k_descale * 1.4426950408889634);
+  p.out_scale = v_descale;
+  Pointers& ptr = res->ptr;
+  ptr.q = q->data;
+  ptr.k = k->data;
+  ptr.v = v->data;
+  ptr.block_table = static_cast<const int32_t*>(bt->data);
+  ptr.seq_lens = static_cast<const int32_t*>(sl->data);
+  ptr.qsl = static_cast<const int32_t*>(qsl->data);
+  ptr.out = out->data;
+  ptr.err = nullptr;
+  return PG_OK;
+}
+
+int run(const Validated& val, const pg_tensor* k, const pg_tensor* v, void* ws, size_t ws_bytes,
+        const WsLayout& L, DeviceState* ds, cudaStream_t stream) {
+  Problem p = val.p;
+  Pointers ptr = val.ptr;
+  ptr.err = ds->err;
+  ClassPlan cp[kNumClasses];
+  for (int c = 0; c < kNumClasses; ++c) cp[c] = class_plan(L, c, static_cast<char*>(ws));
+  (void)ws_bytes;
+  int64_t plan_info[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  cudaError_t e = launch_plan(p, ptr, cp[0], cp[1], stream);
+  if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+  int launched = 1;
+  const int path = g_path.load();
+  // Fast (tcgen05) kernels need an e4m3 cache; bf16 caches use the warp-MMA kernel.
+  const bool fast_ok = path == 0 && p.kv_is_fp8;
+  int used = 0;
+  for (int c = 0; c < kNumClasses; ++c) {
+    bool done = false;
+    cudaEvent_t ev0 = g_ev_start[c].load(), ev1 = g_ev_stop[c].load();
+    if (ev0 && (e = cudaEventRecord(ev0, stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if (fast_ok) {
+      int r = (c == 0) ? launch_verify_tc(p, ptr, cp[c], k, v, ds->sms, stream)
+                       : launch_prefill_tc(p, ptr, cp[c], k, v, ds->sms, stream);
+      if (r < 0) return fail(PG_ERR_CUDA, "tcgen05 %s launch failed: %s", c == 0 ? "verify" : "prefill",
+                             tc_last_error());
+      if (r == 1) {
+        done = true;
+        used |= 2 << c;
+      }
+    }
+    if (!done) {
+      e = launch_portable(p, ptr, cp[c], c == 0 ? kVerifyRows : kPrefillRows, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "portable kernel launch");
+      used |= 8 << c;
+    }
+    ++launched;
+    if (ev1 && (e = cudaEventRecord(ev1, stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  }
+  plan_info[0] = cp[0].num_ctas;
+  plan_info[1] = cp[1].num_ctas;
+  plan_info[2] = launched;
+  plan_info[3] = used;
+  plan_info[4] = cp[0].max_blocks;
+  plan_info[5] = cp[1].max_blocks;
+  plan_info[6] = (int64_t)L.total;
+  memcpy(t_last_plan, plan_info, sizeof plan_info);
+  return PG_OK;
+}
+
+int attn_common(const pg_tensor* q, const pg_tensor* k, const pg_tensor* v, const pg_tensor* bt,
+                const pg_tensor* sl, const pg_tensor* qsl, float q_descale, float k_descale,
+                float v_descale, float softmax_scale, pg_tensor* out, void* user_ws,
+                size_t user_ws_bytes, bool use_user_ws, cudaStream_t stream) {
+  Validated val;
+  int st = validate(q, k, v, bt, sl, qsl, q_descale, k_descale, v_descale, softmax_scale, out, &val);
+  if (st) return st;
+  if (val.p.num_seqs == 0 || val.p.T == 0) {
+    t_last_error.clear();
+    return PG_OK;
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceState* ds = nullptr;
+  if ((st = device_state(dev, &ds))) return st;
+  const WsLayout L = make_layout(val.p.num_seqs, val.p.T, val.p.Hq, val.p.Hkv, ds->sms);
+  void* ws = nullptr;
+  if (use_user_ws) {
+    if (!user_ws || (reinterpret_cast<uintptr_t>(user_ws) & 255u))
+      return fail(PG_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
+    if (user_ws_bytes < L.total)
+      return fail(PG_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", user_ws_bytes, L.total);
+    ws = user_ws;
+    st = run(val, k, v, ws, user_ws_bytes, L, ds, stream);
+  } else {
+    std::lock_guard<std::mutex> lk(ds->mu);
+    if (ds->ws_bytes < L.total) {
+      if (ds->ws) {
+        // Work already queued may still use the old buffer.
+        e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize before workspace growth");
+        cudaFree(ds->ws);
+        ds->ws = nullptr;
+        ds->ws_bytes = 0;
+      }
+      size_t want = L.total + L.total / 4;
+      e = cudaMalloc(&ds->ws, want);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+      ds->ws_bytes = want;
+    }
+    st = run(val, k, v, ds->ws, ds->ws_bytes, L, ds, stream);
+  }
+  if (st == PG_OK) t_last_error.clear();
+  return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_gqa_attn(const pg_tensor* q, const pg_tensor* k_cache, const pg_tensor* v_cache,
+                   const pg_tensor* block_table, const pg_tensor* seq_lens,
+                   const pg_tensor* query_start_loc, float k_descale, float v_descale,
+                   float softmax_scale, pg_tensor* out, pg_stream_t stream) {
+  return attn_common(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, 1.0f, k_descale,
+                     v_descale, softmax_scale, out, nullptr, 0, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int paged_gqa_attn_ex(const pg_tensor* q, const pg_tensor* k_cache, const pg_tensor* v_cache,
+                      const pg_tensor* block_table, const pg_tensor* seq_lens,
+                      const pg_tensor* query_start_loc, float q_descale, float k_descale,
+                      float v_descale, float softmax_scale, pg_tensor* out, void* workspace,
+                      size_t workspace_bytes, pg_stream_t stream) {
+  return attn_common(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, q_descale, k_descale,
+                     v_descale, softmax_scale, out, workspace, workspace_bytes, true,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t paged_gqa_workspace_size(int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
+                                int page_size, int max_blocks_per_seq, int device) {
+  (void)max_blocks_per_seq;
+  if (num_seqs < 0 || total_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_q_heads % num_kv_heads != 0 || page_size <= 0)
+    return 0;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0) return 0;
+  return make_layout(num_seqs, total_q, num_q_heads, num_kv_heads, sms).total;
+}
+
+const char* paged_gqa_last_error(void) { return t_last_error.c_str(); }
+
+int paged_gqa_check_device_errors(pg_stream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceState* ds = nullptr;
+  int st = device_state(dev, &ds);
+  if (st) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof word);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  const uint32_t zero = 0;
+  e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero);
+  if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+  if (word & kErrTimeout) return fail(PG_ERR_TIMEOUT, "device: a bounded wait gave up (word 0x%x)", word);
+  if (word & (kErrBounds | kErrPage))
+    return fail(PG_ERR_DEVICE_BOUNDS, "device: %s%s(word 0x%x)", (word & kErrBounds) ? "sequence bounds " : "",
+                (word & kErrPage) ? "page id out of range " : "", word);
+  t_last_error.clear();
+  return PG_OK;
+}
+
+int paged_gqa_set_path(int path) {
+  if (path < 0 || path > 1) return fail(PG_ERR_INVALID_ARG, "path must be 0 or 1");
+  return g_path.exchange(path);
+}
+
+int paged_gqa_last_plan(int64_t* out8) {
+  if (!out8) return fail(PG_ERR_INVALID_ARG, "null output");
+  memcpy(out8, t_last_plan, sizeof t_last_plan);
+  return PG_OK;
+}
+
+int paged_gqa_set_kernel_events(int cls, void* start, void* stop) {
+  if (cls < 0 || cls >= kNumClasses) return fail(PG_ERR_INVALID_ARG, "class must be 0 or 1");
+  g_ev_start[cls].store(static_cast<cudaEvent_t>(start));
+  g_ev_stop[cls].store(static_cast<cudaEvent_t>(stop));
+  return PG_OK;
+}
+
+int paged_gqa_version(void) { return 100; }
+
+}  // extern "C"

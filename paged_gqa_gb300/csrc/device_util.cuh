@@ -1,0 +1,95 @@
+// device_util.cuh -- small device helpers shared by the attention kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include "common.cuh"
+
+namespace pgqa {
+
+// Row r of a (sequence, kv head) is query token r / G and head kvh*G + r % G.
+struct RowMap {
+  int t, h;
+};
+__device__ __forceinline__ RowMap map_row(int r, int G, int kvh) {
+  RowMap m;
+  m.t = r / G;
+  m.h = kvh * G + (r - m.t * G);
+  return m;
+}
+
+// Two e4m3 codes (low byte = first) -> two floats, exact (the f16 conversion of an
+// e4m3 value is exact, as is f16 -> f32).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float((uint32_t)b << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Partial result slot of (block, split).
+__device__ __forceinline__ float* slot_o(const ClassPlan& cp, int slot) {
+  return cp.part_o + (size_t)slot * kSlotRows * kHeadDim;
+}
+__device__ __forceinline__ float* slot_lse(const ClassPlan& cp, int slot) {
+  return cp.part_lse + (size_t)slot * kSlotRows;
+}
+
+// Called by `nthreads` threads (ids tid = 0..nthreads-1) that share barrier `bar_id`,
+// after each has written its share of this piece's partial result (normalised O and
+// log2-sum-exp per row) and executed __threadfence(). The last piece of a block to
+// arrive merges all pieces of the block:
+//     M = max_i lse_i,  w_i = 2^(lse_i - M),  out = sum_i w_i o_i / sum_i w_i
+// ("Optimize Qwen3.5 MTP unified attention on gfx950": split-KV segments reduced by
+// a second pass). Returns after the merge (if any) is complete.
+__device__ inline void finish_split_block(const Problem& p, const Pointers& ptr, const ClassPlan& cp,
+                                          int block_index, const RowBlock& rb, int tid, int nthreads,
+                                          int bar_id, int* s_flag) {
+  named_barrier(bar_id, nthreads);
+  if (tid == 0) {
+    __threadfence();
+    int old = atomicAdd(&cp.counters[block_index], 1);
+    *s_flag = (old == rb.nsplit - 1);
+    __threadfence();
+  }
+  named_barrier(bar_id, nthreads);
+  if (!*s_flag) return;
+  const int seq_q0 = ptr.qsl[rb.seq];
+  for (int idx = tid; idx < rb.nrows * (kHeadDim / 2); idx += nthreads) {
+    const int r = idx / (kHeadDim / 2);
+    const int d = (idx % (kHeadDim / 2)) * 2;
+    float M = -INFINITY;
+    for (int i = 0; i < rb.nsplit; ++i) M = fmaxf(M, __ldcg(slot_lse(cp, rb.slot_base + i) + r));
+    float wsum = 0.f, a0 = 0.f, a1 = 0.f;
+    for (int i = 0; i < rb.nsplit; ++i) {
+      const float lse = __ldcg(slot_lse(cp, rb.slot_base + i) + r);
+      const float w = (lse == -INFINITY) ? 0.f : exp2f(lse - M);
+      const float2 o = __ldcg(reinterpret_cast<const float2*>(slot_o(cp, rb.slot_base + i) +
+                                                              (size_t)r * kHeadDim + d));
+      wsum += w;
+      a0 += w * o.x;
+      a1 += w * o.y;
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const RowMap m = map_row(rb.row0 + r, p.G, rb.kvh);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(ptr.out) +
+                                                (size_t)(seq_q0 + m.t) * p.o_st +
+                                                (size_t)m.h * p.o_sh + d);
+    *dst = pack_bf16x2(a0 * inv, a1 * inv);
+  }
+}
+
+}  // namespace pgqa

@@ -1,0 +1,171 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Bar (bf16 output): max |diff| <= 1e-2, rel-L2 <= 5e-3, every value finite.
+Unused cache slots are NaN-poisoned in every case, so a kernel that reads a tail
+slot or a spare page fails.
+"""
+import pytest
+import torch
+
+import workloads as wl
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+PATHS = {"auto": 0, "warp_mma": 1}
+
+
+@pytest.fixture(params=list(PATHS))
+def path(request):
+    import paged_gqa_gb300 as pg
+    prev = pg.paged_gqa_set_path(PATHS[request.param])
+    yield request.param
+    pg.paged_gqa_set_path(prev)
+
+
+def _small(seed, **kw):
+    gen = torch.Generator().manual_seed(seed)
+    spec = wl.random_small_spec(gen, **kw)
+    return wl.make_case(spec, device="cuda", seed=seed, poison=True)
+
+
+SMALL_CASES = [
+    # verify shapes (q_len*G <= 64): the MTP packing, several G, both page sizes
+    dict(group=16, num_kv_heads=1, page_size=16, q_lens=[4, 2, 3, 1], max_ctx=700),
+    dict(group=16, num_kv_heads=2, page_size=16, q_lens=[2, 4, 3], max_ctx=1500),
+    dict(group=12, num_kv_heads=2, page_size=64, q_lens=[4, 4, 1, 5], max_ctx=3000),
+    dict(group=8, num_kv_heads=1, page_size=64, q_lens=[8, 1, 0, 3], max_ctx=900),
+    dict(group=1, num_kv_heads=4, page_size=32, q_lens=[1, 2, 4], max_ctx=400),
+    dict(group=3, num_kv_heads=2, page_size=128, q_lens=[2, 6], max_ctx=1000),
+    dict(group=6, num_kv_heads=1, page_size=16, q_lens=[4, 4, 4, 4, 4, 4], max_ctx=260),
+    # prefill shapes (128-row blocks), ragged last block, cached prefix
+    dict(group=8, num_kv_heads=1, page_size=64, q_lens=[300, 17], max_ctx=1200),
+    dict(group=12, num_kv_heads=2, page_size=64, q_lens=[100, 4, 33], max_ctx=800),
+    dict(group=16, num_kv_heads=1, page_size=16, q_lens=[65, 9], max_ctx=400),
+    # bf16 cache
+    dict(group=16, num_kv_heads=1, page_size=16, q_lens=[2, 4], max_ctx=600, kv_dtype="bf16"),
+    dict(group=4, num_kv_heads=2, page_size=64, q_lens=[70, 3], max_ctx=500, kv_dtype="bf16"),
+    # FP8 q
+    dict(group=8, num_kv_heads=1, page_size=64, q_lens=[200, 4], max_ctx=700, q_dtype="e4m3"),
+    dict(group=16, num_kv_heads=1, page_size=16, q_lens=[4, 3], max_ctx=900, q_dtype="e4m3"),
+]
+
+
+@pytest.mark.parametrize("i", range(len(SMALL_CASES)))
+def test_small_cases_match_oracle(i, path):
+    case = _small(1000 + i, **SMALL_CASES[i])
+    got = gu.run_library(case)
+    gu.check_full(case, got, f"case {i} path {path}")
+
+
+def test_config1_tiny_verify(path):
+    case = wl.make_case(wl.config_spec(1), device="cuda", seed=0, poison=True)
+    got = gu.run_library(case)
+    gu.check_full(case, got, "config 1")
+
+
+def test_page_edges_and_no_cache(path):
+    """L exactly on, one past and one short of page boundaries; q_len == L."""
+    seqs = [(4, 16), (4, 17), (4, 15), (3, 3), (1, 1), (4, 128), (4, 129), (2, 255), (40, 40), (4, 4)]
+    spec = wl.CaseSpec("edges", seqs, 16, 1, 16, spare_pages=2)
+    case = wl.make_case(spec, device="cuda", seed=5, poison=True)
+    gu.check_full(case, gu.run_library(case), "page edges")
+
+
+def test_many_short_sequences(path):
+    """More sequences than CTAs, most blocks unsplit."""
+    gen = torch.Generator().manual_seed(9)
+    seqs = [(int(q), int(L)) for q, L in zip(torch.randint(1, 5, (400,), generator=gen),
+                                                torch.randint(4, 300, (400,), generator=gen))]
+    spec = wl.CaseSpec("many", seqs, 16, 1, 16)
+    case = wl.make_case(spec, device="cuda", seed=9, poison=True)
+    gu.check_full(case, gu.run_library(case), "many short")
+
+
+def test_long_single_sequence_is_split(path):
+    """One sequence, one kv head: its keys are cut across all CTAs and merged."""
+    spec = wl.CaseSpec("long", [(4, 40000)], 16, 1, 16)
+    case = wl.make_case(spec, device="cuda", seed=13, poison=True)
+    gu.check_full(case, gu.run_library(case), "long split")
+
+
+def test_output_does_not_depend_on_untouched_rows():
+    """Rows of zero-length queries are not written; everything else is."""
+    spec = wl.CaseSpec("zeroq", [(0, 50), (3, 40), (0, 1), (2, 2)], 8, 1, 16)
+    case = wl.make_case(spec, device="cuda", seed=21, poison=True)
+    got = gu.run_library(case)
+    gu.check_full(case, got, "zero-length queries")
+
+
+def test_strided_views():
+    """Non-packed q/out/cache/block-table strides (views into larger buffers)."""
+    gen = torch.Generator().manual_seed(31)
+    spec = wl.random_small_spec(gen, group=8, num_kv_heads=2, page_size=16, q_lens=[3, 4, 70], max_ctx=500)
+    base = wl.make_case(spec, device="cuda", seed=31, poison=True)
+    T, Hq, D = base.q.shape
+    qbig = torch.zeros(T, Hq + 3, D + 64, dtype=base.q.dtype, device="cuda")
+    qbig[:, :Hq, :D] = base.q
+    NB, P, Hkv, _ = base.k_cache.shape
+    kbig = torch.zeros(NB, P + 1, Hkv + 1, D + 32, dtype=base.k_cache.dtype, device="cuda")
+    kbig[:, :P, :Hkv, :D] = base.k_cache
+    vbig = torch.zeros(NB + 2, P, Hkv, D + 16, dtype=base.v_cache.dtype, device="cuda")
+    vbig[:NB, :, :, :D] = base.v_cache
+    btbig = torch.full((base.block_table.shape[0], base.block_table.shape[1] + 7), -1, dtype=torch.int32, device="cuda")
+    btbig[:, :base.block_table.shape[1]] = base.block_table
+    case = wl.Case(spec, qbig[:, :Hq, :D], kbig[:, :P, :Hkv, :D], vbig[:NB, :, :, :D],
+                   btbig[:, :base.block_table.shape[1]], base.seq_lens, base.query_start_loc,
+                   base.q_descale, base.k_descale, base.v_descale, base.softmax_scale)
+    outbig = torch.full((T, Hq + 1, D + 8), float("nan"), dtype=torch.bfloat16, device="cuda")
+    got = gu.run_library(case, out=outbig[:, :Hq, :D])
+    gu.check_full(base, got.contiguous(), "strided")
+    assert torch.isnan(outbig[:, Hq:, :].float()).all() and torch.isnan(outbig[:, :, D:].float()).all()
+
+
+def test_device_errors_are_flagged_without_trapping():
+    import paged_gqa_gb300 as pg
+    spec = wl.CaseSpec("bad", [(2, 40), (3, 30)], 4, 1, 16)
+    case = wl.make_case(spec, device="cuda", seed=41)
+    # a page id outside [0, NB) for sequence 0
+    bt = case.block_table.clone()
+    bt[0, 1] = case.k_cache.shape[0] + 5
+    bad = wl.Case(spec, case.q, case.k_cache, case.v_cache, bt, case.seq_lens, case.query_start_loc,
+                  case.q_descale, case.k_descale, case.v_descale, case.softmax_scale)
+    gu.run_library(bad, check_errors=False)
+    assert pg.paged_gqa_check_device_errors() == -5
+    # q_len > L for sequence 1: its rows are zeroed, the error is reported
+    sl = case.seq_lens.clone()
+    sl[1] = 2
+    bad = wl.Case(spec, case.q, case.k_cache, case.v_cache, case.block_table, sl, case.query_start_loc,
+                  case.q_descale, case.k_descale, case.v_descale, case.softmax_scale)
+    out = gu.run_library(bad, check_errors=False)
+    assert pg.paged_gqa_check_device_errors() == -5
+    assert (out[2:5].float() == 0).all()
+    # the error word was cleared; a good call reports nothing
+    gu.run_library(case)
+    assert pg.paged_gqa_check_device_errors() == 0
+
+
+def test_caller_workspace_matches_library_workspace():
+    import paged_gqa_gb300 as pg
+    case = _small(77, group=16, num_kv_heads=1, page_size=16, q_lens=[4, 4, 2], max_ctx=5000)
+    ref = gu.run_library(case)
+    spec = case.spec
+    nbytes = pg.paged_gqa_workspace_size(spec.num_seqs, spec.total_q, spec.num_q_heads, spec.num_kv_heads,
+                                         spec.page_size, case.block_table.shape[1], 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(ref)
+    pg.paged_gqa_attn_ex(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                         case.query_start_loc, 1.0, case.k_descale, case.v_descale, case.softmax_scale, out, ws)
+    assert pg.paged_gqa_check_device_errors() == 0
+    assert torch.equal(out, ref)
+    with pytest.raises(pg.PagedGQAError, match="WORKSPACE"):
+        pg.paged_gqa_attn_ex(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                             case.query_start_loc, 1.0, case.k_descale, case.v_descale, case.softmax_scale,
+                             out, ws[: nbytes // 2])
+
+
+def test_deterministic_across_calls():
+    case = _small(88, group=16, num_kv_heads=2, page_size=16, q_lens=[4, 3, 2, 4], max_ctx=9000)
+    a = gu.run_library(case)
+    b = gu.run_library(case)
+    assert torch.equal(a, b)

@@ -266,3 +266,41 @@ def sample_rows(spec: CaseSpec, n_rows: int, seed: int = 0, whole_seqs: Sequence
             extra.extend(range(t * Hq, (t + 1) * Hq))
     rows = torch.cat([picks, torch.tensor(extra, dtype=torch.int64)]) if extra else picks
     return torch.unique(rows)
+
+
+def to_device(case: Case, device="cuda") -> Case:
+    return Case(case.spec, case.q.to(device), case.k_cache.to(device), case.v_cache.to(device),
+                   case.block_table.to(device), case.seq_lens.to(device), case.query_start_loc.to(device),
+                   case.q_descale, case.k_descale, case.v_descale, case.softmax_scale)
+
+
+def subcase(case: Case, seq_ids) -> Case:
+    """The listed sequences alone, with only their pages (sequences are independent)."""
+    spec = case.spec
+    P = spec.page_size
+    qsl = case.query_start_loc.cpu().tolist()
+    sl = case.seq_lens.cpu().tolist()
+    bt = case.block_table.cpu()
+    pages, q_parts, seqs, rows = [], [], [], []
+    for s in seq_ids:
+        n = (sl[s] + P - 1) // P
+        rows.append(list(range(len(pages), len(pages) + n)))
+        pages.extend(bt[s, :n].tolist())
+        q_parts.append(case.q[qsl[s]:qsl[s + 1]].cpu())
+        seqs.append((qsl[s + 1] - qsl[s], sl[s]))
+    idx = torch.tensor(pages, dtype=torch.long, device=case.k_cache.device)
+    k = case.k_cache.index_select(0, idx).cpu()
+    v = case.v_cache.index_select(0, idx).cpu()
+    W = max(1, max(len(r) for r in rows))
+    nbt = torch.full((len(seq_ids), W), -1, dtype=torch.int32)
+    for i, r in enumerate(rows):
+        nbt[i, :len(r)] = torch.tensor(r, dtype=torch.int32)
+    nsl = torch.tensor([L for _, L in seqs], dtype=torch.int32)
+    nqsl = torch.zeros(len(seqs) + 1, dtype=torch.int32)
+    nqsl[1:] = torch.cumsum(torch.tensor([q for q, _ in seqs]), 0).to(torch.int32)
+    sub_spec = CaseSpec(spec.name + "_sub", seqs, spec.num_q_heads, spec.num_kv_heads, P,
+                           q_dtype=spec.q_dtype, kv_dtype=spec.kv_dtype, softmax_scale=spec.softmax_scale)
+    return Case(sub_spec, torch.cat(q_parts, 0), k, v, nbt, nsl, nqsl, case.q_descale, case.k_descale,
+                   case.v_descale, case.softmax_scale)
+
+
