@@ -170,6 +170,9 @@ def paged_gqa_last_plan() -> dict:
 
 def paged_gqa_set_kernel_events(cls: int, start=None, stop=None) -> None:
     """Record torch.cuda.Event pairs around the class-`cls` attention kernel (None clears)."""
+    for e in (start, stop):
+        if e is not None and not e.cuda_event:
+            e.record()  # torch creates the CUDA event lazily, on first record
     h0 = start.cuda_event if start is not None else None
     h1 = stop.cuda_event if stop is not None else None
     _check(load().paged_gqa_set_kernel_events(int(cls), h0, h1))

@@ -165,7 +165,9 @@ plan_kernel(Problem p, Pointers ptr, ClassPlan c0, ClassPlan c1) {
     }
     __syncthreads();
     const long long U = tbase;
-    const int C = cp.num_ctas;
+    // Cut into at most U ranges so that every range is non-empty: a block then has
+    // exactly one piece per range it intersects, and its split count is exact.
+    const int C = (int)min((long long)cp.num_ctas, U);
 
     // ---- per-block split count and partial slots
     int slot_base = 0;
@@ -191,7 +193,7 @@ plan_kernel(Problem p, Pointers ptr, ClassPlan c0, ClassPlan c1) {
 
     // ---- items: count per CTA, scan, fill
     long long ibase = 0;
-    for (int c0i = 0; c0i < C; c0i += blockDim.x) {
+    for (int c0i = 0; c0i < cp.num_ctas; c0i += blockDim.x) {
       int c = c0i + threadIdx.x;
       int cnt = 0, bfirst = 0;
       long long u0 = 0, u1 = 0;
@@ -205,7 +207,7 @@ plan_kernel(Problem p, Pointers ptr, ClassPlan c0, ClassPlan c1) {
         }
       }
       long long pre = block_exclusive_scan(cnt, &s_total) + ibase;
-      if (c < C) {
+      if (c < cp.num_ctas) {
         cp.cta_item_begin[c] = (int)min(pre, (long long)cp.max_items);
         for (int i = 0; i < cnt; ++i) {
           long long ii = pre + i;
@@ -225,7 +227,7 @@ plan_kernel(Problem p, Pointers ptr, ClassPlan c0, ClassPlan c1) {
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      cp.cta_item_begin[C] = (int)min(ibase, (long long)cp.max_items);
+      cp.cta_item_begin[cp.num_ctas] = (int)min(ibase, (long long)cp.max_items);
       *cp.n_blocks = nblocks;
       *cp.n_items = (int)min(ibase, (long long)cp.max_items);
       *cp.total_tiles = U;
