@@ -48,16 +48,19 @@ __device__ __forceinline__ float* slot_lse(const ClassPlan& cp, int slot) {
   return cp.part_lse + (size_t)slot * kSlotRows;
 }
 
+constexpr int kMergeMaxSplits = 16;  // pieces whose weights fit the shared scratch
+
 // Called by `nthreads` threads (ids tid = 0..nthreads-1) that share barrier `bar_id`,
 // after each has written its share of this piece's partial result (normalised O and
 // log2-sum-exp per row) and executed __threadfence(). The last piece of a block to
 // arrive merges all pieces of the block:
-//     M = max_i lse_i,  w_i = 2^(lse_i - M),  out = sum_i w_i o_i / sum_i w_i
+//     M = max_i lse_i,  w_i = 2^(lse_i - M) / sum_j 2^(lse_j - M),  out = sum_i w_i o_i
 // ("Optimize Qwen3.5 MTP unified attention on gfx950": split-KV segments reduced by
-// a second pass). Returns after the merge (if any) is complete.
+// a second pass). s_w is shared scratch of kMergeMaxSplits * kSlotRows floats.
+// Returns after the merge (if any) is complete.
 __device__ inline void finish_split_block(const Problem& p, const Pointers& ptr, const ClassPlan& cp,
                                           int block_index, const RowBlock& rb, int tid, int nthreads,
-                                          int bar_id, int* s_flag) {
+                                          int bar_id, int* s_flag, float* s_w) {
   named_barrier(bar_id, nthreads);
   if (tid == 0) {
     __threadfence();
@@ -67,14 +70,59 @@ __device__ inline void finish_split_block(const Problem& p, const Pointers& ptr,
   }
   named_barrier(bar_id, nthreads);
   if (!*s_flag) return;
+  __threadfence();
   const int seq_q0 = ptr.qsl[rb.seq];
+  const int ns = rb.nsplit;
+  if (ns <= kMergeMaxSplits) {
+    // per-row weights once, then every (row, 4 columns) chunk with independent loads
+    for (int r = tid; r < rb.nrows; r += nthreads) {
+      float lse[kMergeMaxSplits];
+      float M = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kMergeMaxSplits; ++i) {
+        lse[i] = i < ns ? __ldcg(slot_lse(cp, rb.slot_base + i) + r) : -INFINITY;
+        M = fmaxf(M, lse[i]);
+      }
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < kMergeMaxSplits; ++i) {
+        const float w = (lse[i] == -INFINITY) ? 0.f : exp2f(lse[i] - M);
+        lse[i] = w;
+        sum += w;
+      }
+      const float inv = sum > 0.f ? 1.f / sum : 0.f;
+      for (int i = 0; i < ns; ++i) s_w[i * kSlotRows + r] = lse[i] * inv;
+    }
+    named_barrier(bar_id, nthreads);
+#pragma unroll 4
+    for (int idx = tid; idx < rb.nrows * (kHeadDim / 4); idx += nthreads) {
+      const int r = idx / (kHeadDim / 4);
+      const int d = (idx % (kHeadDim / 4)) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i < ns; ++i) {
+        const float w = s_w[i * kSlotRows + r];
+        const float4 o = __ldcg(reinterpret_cast<const float4*>(slot_o(cp, rb.slot_base + i) +
+                                                                (size_t)r * kHeadDim + d));
+        acc.x += w * o.x;
+        acc.y += w * o.y;
+        acc.z += w * o.z;
+        acc.w += w * o.w;
+      }
+      const RowMap m = map_row(rb.row0 + r, p.G, rb.kvh);
+      uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(ptr.out) +
+                                            (size_t)(seq_q0 + m.t) * p.o_st + (size_t)m.h * p.o_sh + d);
+      *dst = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    }
+    named_barrier(bar_id, nthreads);  // s_w may be reused right after
+    return;
+  }
   for (int idx = tid; idx < rb.nrows * (kHeadDim / 2); idx += nthreads) {
     const int r = idx / (kHeadDim / 2);
     const int d = (idx % (kHeadDim / 2)) * 2;
     float M = -INFINITY;
-    for (int i = 0; i < rb.nsplit; ++i) M = fmaxf(M, __ldcg(slot_lse(cp, rb.slot_base + i) + r));
+    for (int i = 0; i < ns; ++i) M = fmaxf(M, __ldcg(slot_lse(cp, rb.slot_base + i) + r));
     float wsum = 0.f, a0 = 0.f, a1 = 0.f;
-    for (int i = 0; i < rb.nsplit; ++i) {
+    for (int i = 0; i < ns; ++i) {
       const float lse = __ldcg(slot_lse(cp, rb.slot_base + i) + r);
       const float w = (lse == -INFINITY) ? 0.f : exp2f(lse - M);
       const float2 o = __ldcg(reinterpret_cast<const float2*>(slot_o(cp, rb.slot_base + i) +

@@ -24,7 +24,8 @@ constexpr int kPWarps = 8;
 constexpr int kPThreads = kPWarps * 32;
 constexpr int kPKeys = 32;
 constexpr int kPitch = kHeadDim + 4;  // floats; keeps fragment loads conflict-free
-constexpr size_t kPSmemBytes = (size_t)(kPrefillRows + 2 * kPKeys) * kPitch * sizeof(float);
+constexpr size_t kPSmemBytes = (size_t)(kPrefillRows + 2 * kPKeys) * kPitch * sizeof(float) +
+                               (size_t)kMergeMaxSplits * kSlotRows * sizeof(float);
 
 __device__ __forceinline__ uint32_t to_tf32(float x) {
   uint32_t r;
@@ -272,7 +273,7 @@ portable_attn_kernel(Problem p, Pointers ptr, ClassPlan cp) {
         }
       }
       __threadfence();
-      finish_split_block(p, ptr, cp, item.block, rb, tid, kPThreads, 1, &s_flag);
+      finish_split_block(p, ptr, cp, item.block, rb, tid, kPThreads, 1, &s_flag, Vs + kPKeys * kPitch);
       __syncthreads();
     }
   }

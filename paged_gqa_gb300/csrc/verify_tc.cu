@@ -10,7 +10,7 @@
 //   * swap-AB: the 128 keys of a tile are the MMA's M dimension and the (padded) 64 query
 //     rows are N, so a 64-row verify block fills the 128-lane tensor core. S^T = K Q^T and
 //     O^T += V^T P^T, both tcgen05.mma kind::f8f6f4 with fp32 accumulators in TMEM;
-//   * FP8 K and V go from HBM to shared memory by TMA (one 2-D box per page and d-half,
+//   * FP8 K and V go from HBM to shared memory by TMA (one box per page and d-half,
 //     addressed through the block table) and into the MMA untouched; the dequant scales are
 //     folded into the score scale (k_descale) and the output scale (v_descale);
 //   * bf16 Q is split once per block into e4m3 hi + lo parts (q*2^s = hi + lo, exact to
@@ -24,8 +24,11 @@
 //   * persistent CTAs (one per SM) walk a contiguous range of key tiles cut by the plan
 //     kernel; a block cut across CTAs is finished by the last piece with a log-sum-exp merge.
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer (+ TMEM owner),
-// warps 2-5 = softmax and epilogue (thread i <-> TMEM lane i <-> key i of the tile).
+// Warp roles (352 threads): warp 0 = K producer (TMA), warp 1 = MMA issuer (+ TMEM owner),
+// warps 2-9 = softmax and epilogue, warp 10 = V producer (TMA). Softmax thread (q, c, lane)
+// owns TMEM lane 32q+lane (= key of the tile, = d within a d-half for O^T) and rows
+// [32c, 32c+32). Shared memory: Q hi/lo 32 KB, 2 K stages and 3 V stages of 32 KB, P hi/lo
+// 16 KB, barriers and row state (~221 KB, one CTA per SM).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -47,8 +50,13 @@ namespace {
 using namespace tc;
 
 constexpr int kVN = 64;            // MMA N: query rows, padded
-constexpr int kVThreads = 192;
-constexpr int kStages = 2;         // K/V shared-memory stages
+constexpr int kSoftWarps = 8;
+constexpr int kSoftThreads = kSoftWarps * 32;
+constexpr int kVThreads = 96 + kSoftThreads;  // + K producer, MMA, V producer warps
+constexpr int kVProducerWarp = 2 + kSoftWarps;
+constexpr int kCols = kVN / 2;     // rows per softmax thread
+constexpr int kKStages = 2;        // K tiles in shared memory (freed by S = K Q^T)
+constexpr int kVStages = 3;        // V tiles in shared memory (held until O += P V)
 constexpr float kTau = 4.f;        // rescale when a score exceeds the reference by 2^kTau
 constexpr float kSigma = 4.f;      // P is stored scaled by 2^kSigma (max 2^(kTau+kSigma) = 256)
 constexpr float kMInit = -1.0e30f; // reference of a row before its first key
@@ -61,8 +69,8 @@ constexpr uint32_t kPPart = kTileKeys * kVN;    // [128 keys][64 B]
 constexpr uint32_t kOffQhi = 0;
 constexpr uint32_t kOffQlo = kOffQhi + kQPart;
 constexpr uint32_t kOffK = kOffQlo + kQPart;
-constexpr uint32_t kOffV = kOffK + kStages * kKVTile;
-constexpr uint32_t kOffPhi = kOffV + kStages * kKVTile;
+constexpr uint32_t kOffV = kOffK + kKStages * kKVTile;
+constexpr uint32_t kOffPhi = kOffV + kVStages * kKVTile;
 constexpr uint32_t kOffPlo = kOffPhi + kPPart;
 constexpr uint32_t kOffMisc = kOffPlo + kPPart;
 
@@ -82,13 +90,15 @@ struct Misc {
   alignas(16) float lrow[kVN];
   alignas(16) int lim[2][kVN];
   alignas(16) long long out_off[2][kVN];
-  alignas(8) uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
+  alignas(16) float merge_w[kMergeMaxSplits * kSlotRows];
+  alignas(8) uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full, p_free, q_full, q_free, o_ready, o_free, drain;
   float qscale[2];
+  float amax[kSoftWarps];
   uint32_t tmem_base;
   int abort_flag;
-  int vote[2][4];
+  int vote[2][kSoftWarps];
   int merge_flag;
 };
 static_assert(offsetof(Misc, m) % 16 == 0 && offsetof(Misc, k_full) % 8 == 0, "Misc alignment");
@@ -154,22 +164,24 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   auto bar = [&](const uint64_t& b) { return smem_u32(&b); };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(bar(ms.k_full[s]), 1);
-      mbar_init(bar(ms.v_full[s]), 1);
       mbar_init(bar(ms.k_empty[s]), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(bar(ms.v_full[s]), 1);
       mbar_init(bar(ms.v_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(ms.s_full[b]), 1);
-      mbar_init(bar(ms.s_free[b]), 128);
+      mbar_init(bar(ms.s_free[b]), kSoftThreads);
     }
-    mbar_init(bar(ms.p_full), 128);
+    mbar_init(bar(ms.p_full), kSoftThreads);
     mbar_init(bar(ms.p_free), 1);
-    mbar_init(bar(ms.q_full), 128);
+    mbar_init(bar(ms.q_full), kSoftThreads);
     mbar_init(bar(ms.q_free), 1);
     mbar_init(bar(ms.o_ready), 1);
-    mbar_init(bar(ms.o_free), 128);
+    mbar_init(bar(ms.o_free), kSoftThreads);
     mbar_init(bar(ms.drain), 1);
     ms.abort_flag = 0;
     fence_mbar_init();
@@ -183,25 +195,33 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmap_k);
-      tma_prefetch_desc(&tmap_v);
-    }
+  if (warp == 0 || warp == kVProducerWarp) {
+    // ------------------------------------------------------------ TMA producers (K, V)
+    // Two independent warps, so K tiles run ahead as soon as S = K Q^T frees a stage,
+    // whatever the P.V of older tiles is doing.
+    const bool is_k = warp == 0;
+    const CUtensorMap* tmap = is_k ? &tmap_k : &tmap_v;
+    const int nst = is_k ? kKStages : kVStages;
+    const uint32_t region = sbase + (is_k ? kOffK : kOffV);
+    uint64_t* full = is_k ? ms.k_full : ms.v_full;
+    uint64_t* empty = is_k ? ms.k_empty : ms.v_empty;
+    if (lane == 0) tma_prefetch_desc(tmap);
     const uint64_t policy = policy_evict_first();
-    const int ppt = kTileKeys / p.P;  // pages per tile (1..8)
+    const int ppt = kTileKeys / p.P;  // pages per tile (1, 2, 4 or 8); 32 is a multiple
     uint32_t g = 0;
-    uint32_t issued_k[kStages] = {}, issued_v[kStages] = {};
+    uint32_t issued[kVStages] = {};
     bool stop = false;
     for (int it = item_begin; it < item_end && !stop; ++it) {
       const Item I = load_item(cp, ptr, it);
       const int32_t* bt_row = ptr.block_table + (size_t)I.seq * p.bt_stride;
-      auto fetch = [&](int j) -> int {
-        const int key0 = (I.tile_begin + j) * kTileKeys + lane * p.P;
+      const int page0 = I.tile_begin * ppt;                 // first page of the piece
+      const int npages = (I.kv_hi + p.P - 1) / p.P - page0; // pages the piece reads
+      // a window of 32 block-table entries, one per lane, and the next one in flight
+      auto fetch = [&](int w) -> int {
+        const int pg = w * 32 + lane;
         int blk = -1;
-        if (lane < ppt && key0 < I.kv_hi) {
-          blk = bt_row[key0 / p.P];
+        if (pg < npages) {
+          blk = bt_row[page0 + pg];
           if (blk < 0 || blk >= p.NB) {
             atomicOr(ptr.err, kErrPage);
             blk = 0;
@@ -209,46 +229,43 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
         return blk;
       };
-      int cur = fetch(0);
+      int cur = fetch(0), nxt = fetch(1);
+      int cur_w = 0;
       for (int j = 0; j < I.ntiles; ++j, ++g) {
-        const int nxt = (j + 1 < I.ntiles) ? fetch(j + 1) : -1;
-        const uint32_t st = g % kStages, ph = (g / kStages) & 1;
-        const int npages = __popc(__ballot_sync(0xffffffffu, cur >= 0));
+        const int first = j * ppt;  // page of this tile, relative to the piece
+        if (first / 32 != cur_w) {
+          cur = nxt;
+          cur_w = first / 32;
+          nxt = fetch(cur_w + 1);
+        }
+        const int tile_pages = min(ppt, npages - first);
+        const uint32_t st = g % nst, ph = (g / nst) & 1;
         int ok = 1;
         if (lane == 0) {
-          const uint32_t bytes = (uint32_t)npages * p.P * 128u * 2u;
-          ok = mbar_wait(bar(ms.k_empty[st]), ph ^ 1, abort_flag, ptr.err);
-          if (ok) mbar_expect_tx(bar(ms.k_full[st]), bytes);
-          if (ok) ok = mbar_wait(bar(ms.v_empty[st]), ph ^ 1, abort_flag, ptr.err);
-          if (ok) mbar_expect_tx(bar(ms.v_full[st]), bytes);
+          ok = mbar_wait(bar(empty[st]), ph ^ 1, abort_flag, ptr.err);
+          if (ok) mbar_expect_tx(bar(full[st]), (uint32_t)tile_pages * p.P * 128u * 2u);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) {
           stop = true;
           break;
         }
-        for (int pg = 0; pg < npages; ++pg) {
-          const int blk = __shfl_sync(0xffffffffu, cur, pg);
+        for (int pg = 0; pg < tile_pages; ++pg) {
+          const int blk = __shfl_sync(0xffffffffu, cur, (first + pg) & 31);
           if (lane == 0) {
             const uint32_t row = (uint32_t)pg * p.P * 128u;
-            for (int h = 0; h < 2; ++h) {
-              tma_load_4d(sbase + kOffK + st * kKVTile + h * kKVHalf + row, &tmap_k, h * 128, I.kvh, 0, blk,
-                          bar(ms.k_full[st]), policy);
-              tma_load_4d(sbase + kOffV + st * kKVTile + h * kKVHalf + row, &tmap_v, h * 128, I.kvh, 0, blk,
-                          bar(ms.v_full[st]), policy);
-            }
+            for (int h = 0; h < 2; ++h)
+              tma_load_4d(region + st * kKVTile + h * kKVHalf + row, tmap, h * 128, I.kvh, 0, blk, bar(full[st]),
+                          policy);
           }
         }
-        issued_k[st] = issued_v[st] = g / kStages + 1;
-        cur = nxt;
+        issued[st] = g / nst + 1;
       }
     }
     // Every issued copy has landed before the CTA may exit.
     if (lane == 0) {
-      for (int s = 0; s < kStages; ++s) {
-        if (issued_k[s]) mbar_wait(bar(ms.k_full[s]), (issued_k[s] - 1) & 1, abort_flag, ptr.err);
-        if (issued_v[s]) mbar_wait(bar(ms.v_full[s]), (issued_v[s] - 1) & 1, abort_flag, ptr.err);
-      }
+      for (int s = 0; s < nst; ++s)
+        if (issued[s]) mbar_wait(bar(full[s]), (issued[s] - 1) & 1, abort_flag, ptr.err);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -264,8 +281,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       auto issue_pv = [&](const Pending& t) -> bool {
         if (t.first && t.item >= 1 && !mbar_wait(bar(ms.o_free), (t.item - 1) & 1, abort_flag, ptr.err)) return false;
         if (!mbar_wait(bar(ms.p_full), t.g & 1, abort_flag, ptr.err)) return false;
-        const uint32_t st = t.g % kStages;
-        if (!mbar_wait(bar(ms.v_full[st]), (t.g / kStages) & 1, abort_flag, ptr.err)) return false;
+        const uint32_t st = t.g % kVStages;
+        if (!mbar_wait(bar(ms.v_full[st]), (t.g / kVStages) & 1, abort_flag, ptr.err)) return false;
         tc_fence_after();
         for (int h = 0; h < 2; ++h) {
           for (int part = 0; part < 2; ++part) {
@@ -285,8 +302,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         const Item I = load_item(cp, ptr, it);
         for (int j = 0; j < I.ntiles && ok; ++j, ++g) {
           if (j == 0 && !(ok = mbar_wait(bar(ms.q_full), ii & 1, abort_flag, ptr.err))) break;
-          const uint32_t st = g % kStages, b = g & 1;
-          if (!(ok = mbar_wait(bar(ms.k_full[st]), (g / kStages) & 1, abort_flag, ptr.err))) break;
+          const uint32_t st = g % kKStages, b = g & 1;
+          if (!(ok = mbar_wait(bar(ms.k_full[st]), (g / kKStages) & 1, abort_flag, ptr.err))) break;
           if (g >= 2 && !(ok = mbar_wait(bar(ms.s_free[b]), ((g >> 1) - 1) & 1, abort_flag, ptr.err))) break;
           tc_fence_after();
           const int parts = kQFp8 ? 1 : 2;
@@ -311,22 +328,24 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       mbar_wait(bar(ms.drain), 0, abort_flag, ptr.err);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2 && warp < kVProducerWarp) {
     // ------------------------------------------------------------ softmax + epilogue
+    const int sw = warp - 2;                 // 0..7
+    const int gi = sw * 32 + lane;           // 0..255
     const int q4 = warp & 3;                 // TMEM lane quarter
+    const int c0 = (sw >> 2) * kCols;        // first row (column) this thread owns
     const int ti = q4 * 32 + lane;           // TMEM lane = key in tile = d in half
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
-    const size_t qesz = kQFp8 ? 1 : 2;
-    float l[kVN];
+    float l[kCols];
 #pragma unroll
-    for (int n = 0; n < kVN; ++n) l[n] = 0.f;
+    for (int n = 0; n < kCols; ++n) l[n] = 0.f;
     bool bad = false;
 
     auto q_prep = [&](const Item& I, int ii) {
       const int pi = ii & 1;
       if (ii >= 1 && !mbar_wait(bar(ms.q_free), (ii - 1) & 1, abort_flag, ptr.err)) bad = true;
-      if (ti < kVN) {
-        const int n = ti;
+      if (gi < kVN) {
+        const int n = gi;
         if (n < I.nrows) {
           const RowMap m = map_row(I.row0 + n, p.G, I.kvh);
           ms.lim[pi][n] = I.L - I.qn + m.t;
@@ -338,69 +357,79 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         // padding rows: a finite reference, so their (discarded) scores never vote
         ms.m[pi][n] = n < I.nrows ? kMInit : 0.f;
       }
-      // rows x 16 chunks of 16 elements
+      // 64 rows x 16 chunks of 16 elements; thread gi takes chunks gi + 256k, k < 4
       auto src_of = [&](int r, int ch) -> const uint8_t* {
         const RowMap m = map_row(I.row0 + r, p.G, I.kvh);
         return static_cast<const uint8_t*>(ptr.q) +
-               ((size_t)(I.q0 + m.t) * p.q_st + (size_t)m.h * p.q_sh + ch * 16) * qesz;
+               ((size_t)(I.q0 + m.t) * p.q_st + (size_t)m.h * p.q_sh + ch * 16) * (kQFp8 ? 1 : 2);
       };
       auto dst_of = [&](uint32_t part_off, int r, int ch) -> uint8_t* {
         const int h = ch >> 3, c = ch & 7;
         return smem + part_off + h * kQHalf + r * 128 + ((c ^ (r & 7)) << 4);
       };
       if (kQFp8) {
-        for (int c = ti; c < kVN * 16; c += 128) {
-          const int r = c >> 4, ch = c & 15;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (r < I.nrows) v = *reinterpret_cast<const uint4*>(src_of(r, ch));
-          *reinterpret_cast<uint4*>(dst_of(kOffQhi, r, ch)) = v;
+        uint4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = gi + k * kSoftThreads, r = c >> 4, ch = c & 15;
+          v[k] = r < I.nrows ? *reinterpret_cast<const uint4*>(src_of(r, ch)) : make_uint4(0, 0, 0, 0);
         }
-        if (ti == 0) ms.qscale[pi] = 1.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = gi + k * kSoftThreads, r = c >> 4, ch = c & 15;
+          *reinterpret_cast<uint4*>(dst_of(kOffQhi, r, ch)) = v[k];
+        }
+        if (gi == 0) ms.qscale[pi] = 1.f;
       } else {
+        uint4 v[4][2];
         float amax = 0.f;
-        for (int c = ti; c < kVN * 16; c += 128) {
-          const int r = c >> 4, ch = c & 15;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = gi + k * kSoftThreads, r = c >> 4, ch = c & 15;
           if (r < I.nrows) {
             const uint4* s = reinterpret_cast<const uint4*>(src_of(r, ch));
-            const uint4 a = s[0], b = s[1];
-            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            v[k][0] = s[0];
+            v[k][1] = s[1];
+          } else {
+            v[k][0] = v[k][1] = make_uint4(0, 0, 0, 0);
+          }
+        }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float2 f = bf2(w[i]);
-              amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-            }
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t w[8] = {v[k][0].x, v[k][0].y, v[k][0].z, v[k][0].w,
+                                 v[k][1].x, v[k][1].y, v[k][1].z, v[k][1].w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float2 f = bf2(w[i]);
+            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
           }
         }
         amax = warp_max(amax);
-        if (lane == 0) ms.red[q4][0] = amax;
-        named_barrier(1, 128);
-        amax = fmaxf(fmaxf(ms.red[0][0], ms.red[1][0]), fmaxf(ms.red[2][0], ms.red[3][0]));
-        named_barrier(1, 128);
+        if (lane == 0) ms.amax[sw] = amax;
+        named_barrier(1, kSoftThreads);
+        amax = 0.f;
+#pragma unroll
+        for (int w = 0; w < kSoftWarps; ++w) amax = fmaxf(amax, ms.amax[w]);
         // 2^sig * amax in [128, 256): exponent arithmetic on the bits
         int sig = 0;
         if (amax > 0.f && isfinite(amax)) sig = 7 - (int)((__float_as_uint(amax) >> 23) & 0xff) + 127;
         sig = max(-100, min(100, sig));
         const float scale = ldexpf(1.f, sig);
-        for (int c = ti; c < kVN * 16; c += 128) {
-          const int r = c >> 4, ch = c & 15;
-          uint4 hv = make_uint4(0, 0, 0, 0), lv = make_uint4(0, 0, 0, 0);
-          if (r < I.nrows) {
-            const uint4* s = reinterpret_cast<const uint4*>(src_of(r, ch));
-            const uint4 a = s[0], b = s[1];
-            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            uint32_t hw[4], lw[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 f0 = bf2(w[2 * i]), f1 = bf2(w[2 * i + 1]);
-              split4(f0.x * scale, f0.y * scale, f1.x * scale, f1.y * scale, hw[i], lw[i]);
-            }
-            hv = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            lv = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        for (int k = 0; k < 4; ++k) {
+          const int c = gi + k * kSoftThreads, r = c >> 4, ch = c & 15;
+          const uint32_t w[8] = {v[k][0].x, v[k][0].y, v[k][0].z, v[k][0].w,
+                                 v[k][1].x, v[k][1].y, v[k][1].z, v[k][1].w};
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f0 = bf2(w[2 * i]), f1 = bf2(w[2 * i + 1]);
+            split4(f0.x * scale, f0.y * scale, f1.x * scale, f1.y * scale, hw[i], lw[i]);
           }
-          *reinterpret_cast<uint4*>(dst_of(kOffQhi, r, ch)) = hv;
-          *reinterpret_cast<uint4*>(dst_of(kOffQlo, r, ch)) = lv;
+          *reinterpret_cast<uint4*>(dst_of(kOffQhi, r, ch)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(dst_of(kOffQlo, r, ch)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
-        if (ti == 0) ms.qscale[pi] = ldexpf(1.f, -sig);
+        if (gi == 0) ms.qscale[pi] = ldexpf(1.f, -sig);
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(ms.q_full));
@@ -408,32 +437,27 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 
     int ii = 0;
     uint32_t g = 0;
-    const int n_items = item_end - item_begin;
-    if (n_items > 0) q_prep(load_item(cp, ptr, item_begin), 0);
+    if (item_end > item_begin) q_prep(load_item(cp, ptr, item_begin), 0);
     for (int it = item_begin; it < item_end; ++it, ++ii) {
       const Item I = load_item(cp, ptr, it);
       const int pi = ii & 1;
-      named_barrier(1, 128);  // q_prep's shared writes (lim, m, qscale) are visible
+      named_barrier(1, kSoftThreads);  // q_prep's shared writes (lim, m, qscale) are visible
       const float c = p.score_scale_log2 * ms.qscale[pi];
-      int min_lim = 0x7fffffff;
-      {
-        const RowMap m0 = map_row(I.row0, p.G, I.kvh);
-        min_lim = I.L - I.qn + m0.t;
-      }
+      const int min_lim = I.L - I.qn + map_row(I.row0, p.G, I.kvh).t;
       bool aborted = false;
       for (int j = 0; j < I.ntiles; ++j, ++g) {
         const int b = g & 1;
         const int key0 = (I.tile_begin + j) * kTileKeys;
         const int key = key0 + ti;
-        float t[kVN];
+        float t[kCols];
         if (!mbar_wait(bar(ms.s_full[b]), (g >> 1) & 1, abort_flag, ptr.err)) bad = true;
         tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < kVN; c0 += 16) {
+        for (int k = 0; k < kCols; k += 16) {
           float v[16];
-          tmem_ld16(tmem + lane_addr + kColS + b * kVN + c0, v);
+          tmem_ld16(tmem + lane_addr + kColS + b * kVN + c0 + k, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) t[c0 + i] = v[i];
+          for (int i = 0; i < 16; ++i) t[k + i] = v[i];
         }
         tmem_wait_ld();
         tc_fence_before();
@@ -442,26 +466,28 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         if (need_mask) {
           const bool kin = key < I.kv_hi;
 #pragma unroll
-          for (int n = 0; n < kVN; ++n) {
-            const bool vis = kin && key <= ms.lim[pi][n];
+          for (int n = 0; n < kCols; ++n) {
+            const bool vis = kin && key <= ms.lim[pi][c0 + n];
             t[n] = vis ? t[n] * c : -INFINITY;
           }
         } else {
 #pragma unroll
-          for (int n = 0; n < kVN; ++n) t[n] = t[n] * c;
+          for (int n = 0; n < kCols; ++n) t[n] = t[n] * c;
         }
         // vote: does any score exceed its row reference by more than 2^kTau?
         bool mine = false;
 #pragma unroll
-        for (int n = 0; n < kVN; n += 4) {
-          const float4 m4 = *reinterpret_cast<const float4*>(&ms.m[pi][n]);
+        for (int n = 0; n < kCols; n += 4) {
+          const float4 m4 = *reinterpret_cast<const float4*>(&ms.m[pi][c0 + n]);
           mine |= (t[n] - m4.x > kTau) | (t[n + 1] - m4.y > kTau) | (t[n + 2] - m4.z > kTau) |
                   (t[n + 3] - m4.w > kTau);
         }
         const int wv = (__any_sync(0xffffffffu, mine) ? 1 : 0) | ((bad || *abort_flag) ? 2 : 0);
-        if (lane == 0) ms.vote[g & 1][q4] = wv;
-        named_barrier(1, 128);
-        const int votes = ms.vote[g & 1][0] | ms.vote[g & 1][1] | ms.vote[g & 1][2] | ms.vote[g & 1][3];
+        if (lane == 0) ms.vote[g & 1][sw] = wv;
+        named_barrier(1, kSoftThreads);
+        int votes = 0;
+#pragma unroll
+        for (int w = 0; w < kSoftWarps; ++w) votes |= ms.vote[g & 1][w];
         if (votes & 2) {
           aborted = true;
           break;
@@ -469,28 +495,28 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         const bool rescale = votes & 1;
         if (rescale) {
 #pragma unroll
-          for (int n = 0; n < kVN; ++n) {
+          for (int n = 0; n < kCols; ++n) {
             const float r = warp_max(t[n]);
-            if (lane == (n & 31)) ms.red[q4][n] = r;
+            if (lane == n) ms.red[q4][c0 + n] = r;
           }
-          named_barrier(1, 128);
-          if (ti < kVN) {
-            const int n = ti;
+          named_barrier(1, kSoftThreads);
+          if (gi < kVN) {
+            const int n = gi;
             const float mt = fmaxf(fmaxf(ms.red[0][n], ms.red[1][n]), fmaxf(ms.red[2][n], ms.red[3][n]));
             const float mo = ms.m[pi][n];
             const float mn = fmaxf(mo, mt);
             ms.alpha[n] = ex2(mo - mn);
             ms.m[pi][n] = mn;
           }
-          named_barrier(1, 128);
+          named_barrier(1, kSoftThreads);
 #pragma unroll
-          for (int n = 0; n < kVN; ++n) l[n] *= ms.alpha[n];
+          for (int n = 0; n < kCols; ++n) l[n] *= ms.alpha[c0 + n];
         }
         // P = 2^(t - m + sigma), split into e4m3 hi + lo, 4 rows per word
-        uint32_t ph[kVN / 4], pl[kVN / 4];
+        uint32_t ph[kCols / 4], pl[kCols / 4];
 #pragma unroll
-        for (int n = 0; n < kVN; n += 4) {
-          const float4 m4 = *reinterpret_cast<const float4*>(&ms.m[pi][n]);
+        for (int n = 0; n < kCols; n += 4) {
+          const float4 m4 = *reinterpret_cast<const float4*>(&ms.m[pi][c0 + n]);
           const float p0 = ex2(t[n] - m4.x + kSigma), p1 = ex2(t[n + 1] - m4.y + kSigma);
           const float p2 = ex2(t[n + 2] - m4.z + kSigma), p3 = ex2(t[n + 3] - m4.w + kSigma);
           l[n] += p0;
@@ -506,13 +532,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll 1
           for (int h = 0; h < 2; ++h) {
 #pragma unroll 1
-            for (int c0 = 0; c0 < kVN; c0 += 16) {
+            for (int k = 0; k < kCols; k += 16) {
               float v[16];
-              const uint32_t a = tmem + lane_addr + kColO + h * kVN + c0;
+              const uint32_t a = tmem + lane_addr + kColO + h * kVN + c0 + k;
               tmem_ld16(a, v);
               tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] *= ms.alpha[c0 + i];
+              for (int i = 0; i < 16; ++i) v[i] *= ms.alpha[c0 + k + i];
               tmem_st16(a, v);
             }
           }
@@ -520,26 +546,27 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
         if (key0 + kTileKeys > I.kv_hi) {
           // keys past the piece's end: their V rows (stale or NaN slots) become zeros
-          const uint32_t st = g % kStages;
-          if (!mbar_wait(bar(ms.v_full[st]), (g / kStages) & 1, abort_flag, ptr.err)) bad = true;
+          const uint32_t st = g % kVStages;
+          if (!mbar_wait(bar(ms.v_full[st]), (g / kVStages) & 1, abort_flag, ptr.err)) bad = true;
           if (key >= I.kv_hi) {
-            uint4 z = make_uint4(0, 0, 0, 0);
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            // this thread zeroes its row's d-half (c0 == 0 -> d 0..127, else 128..255)
+            uint4* row = reinterpret_cast<uint4*>(smem + kOffV + st * kKVTile + (c0 ? kKVHalf : 0) + ti * 128);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint4* row = reinterpret_cast<uint4*>(smem + kOffV + st * kKVTile + h * kKVHalf + ti * 128);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) row[i] = z;
-            }
+            for (int i = 0; i < 8; ++i) row[i] = z;
           }
         }
-        // store P^T rows: key ti, 64 bytes per part, 64-byte swizzle
+        // P^T rows: key ti, rows [c0, c0+32) of each part, 64-byte swizzle
         {
-          const int sw = (ti >> 1) & 3;
+          const int swz = (ti >> 1) & 3;
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const uint32_t off = ti * 64 + ((cc ^ sw) << 4);
-            *reinterpret_cast<uint4*>(smem + kOffPhi + off) = make_uint4(ph[4 * cc], ph[4 * cc + 1], ph[4 * cc + 2], ph[4 * cc + 3]);
-            *reinterpret_cast<uint4*>(smem + kOffPlo + off) = make_uint4(pl[4 * cc], pl[4 * cc + 1], pl[4 * cc + 2], pl[4 * cc + 3]);
+          for (int cc = 0; cc < 2; ++cc) {
+            const int chunk = (c0 >> 4) + cc;
+            const uint32_t off = ti * 64 + ((chunk ^ swz) << 4);
+            *reinterpret_cast<uint4*>(smem + kOffPhi + off) =
+                make_uint4(ph[4 * cc], ph[4 * cc + 1], ph[4 * cc + 2], ph[4 * cc + 3]);
+            *reinterpret_cast<uint4*>(smem + kOffPlo + off) =
+                make_uint4(pl[4 * cc], pl[4 * cc + 1], pl[4 * cc + 2], pl[4 * cc + 3]);
           }
         }
         fence_proxy_async_smem();
@@ -553,13 +580,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       // ---------------------------------------------------------- epilogue
       if (!mbar_wait(bar(ms.o_ready), ii & 1, abort_flag, ptr.err)) bad = true;
       tc_fence_after();
-      // row sums: reduce l over the 128 key lanes (warp reduce-scatter, then across warps)
+      // row sums: reduce l over the 128 key lanes (warp reduce-scatter, then across quarters)
       {
-        float v[kVN];
+        float v[kCols];
 #pragma unroll
-        for (int n = 0; n < kVN; ++n) v[n] = l[n];
+        for (int n = 0; n < kCols; ++n) v[n] = l[n];
 #pragma unroll
-        for (int w = 32, o = 16; o >= 1; w >>= 1, o >>= 1) {
+        for (int w = 16, o = 16; o >= 1; w >>= 1, o >>= 1) {
           const bool up = lane & o;
 #pragma unroll
           for (int i = 0; i < w; ++i) {
@@ -568,33 +595,32 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
           }
         }
-        // lane now holds rows 2*lane and 2*lane+1
-        ms.red[q4][2 * lane] = v[0];
-        ms.red[q4][2 * lane + 1] = v[1];
+        // lane now holds row c0 + lane
+        ms.red[q4][c0 + lane] = v[0];
       }
-      named_barrier(1, 128);
-      if (ti < kVN) {
-        const int n = ti;
+      named_barrier(1, kSoftThreads);
+      if (gi < kVN) {
+        const int n = gi;
         ms.lrow[n] = ms.red[0][n] + ms.red[1][n] + ms.red[2][n] + ms.red[3][n];
       }
-      named_barrier(1, 128);
+      named_barrier(1, kSoftThreads);
       const bool split = I.nsplit > 1;
       const int slot = I.slot_base + I.split;
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < kVN; c0 += 16) {
-          if (c0 >= I.nrows) break;
+        for (int k = 0; k < kCols; k += 16) {
+          if (c0 + k >= I.nrows) break;
           float v[16];
-          tmem_ld16(tmem + lane_addr + kColO + h * kVN + c0, v);
+          tmem_ld16(tmem + lane_addr + kColO + h * kVN + c0 + k, v);
           tmem_wait_ld();
+          const int d = h * 128 + ti;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int n = c0 + i;
+            const int n = c0 + k + i;
             if (n < I.nrows) {
               const float lr = ms.lrow[n];
               const float val = lr > 0.f ? v[i] * (p.out_scale / lr) : 0.f;
-              const int d = h * 128 + ti;
               if (split) {
                 slot_o(cp, slot)[(size_t)n * kHeadDim + d] = val;
               } else {
@@ -607,9 +633,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       tc_fence_before();
       mbar_arrive(bar(ms.o_free));
       if (split) {
-        if (ti < I.nrows) {
-          const float lr = ms.lrow[ti];
-          slot_lse(cp, slot)[ti] = lr > 0.f ? ms.m[pi][ti] - kSigma + log2f(lr) : -INFINITY;
+        if (gi < I.nrows) {
+          const float lr = ms.lrow[gi];
+          slot_lse(cp, slot)[gi] = lr > 0.f ? ms.m[pi][gi] - kSigma + log2f(lr) : -INFINITY;
         }
         __threadfence();
         RowBlock rb;
@@ -619,10 +645,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         rb.nrows = I.nrows;
         rb.nsplit = I.nsplit;
         rb.slot_base = I.slot_base;
-        finish_split_block(p, ptr, cp, I.block, rb, ti, 128, 2, &ms.merge_flag);
+        finish_split_block(p, ptr, cp, I.block, rb, gi, kSoftThreads, 2, &ms.merge_flag, ms.merge_w);
       }
 #pragma unroll
-      for (int n = 0; n < kVN; ++n) l[n] = 0.f;
+      for (int n = 0; n < kCols; ++n) l[n] = 0.f;
     }
   }
 
@@ -651,7 +677,8 @@ EncodeTiledFn encode_fn() {
   if (!fn) {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &f, cudaEnableDefault, &q) == cudaSuccess &&
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<EncodeTiledFn>(f);
   }
@@ -660,12 +687,14 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
+void set_tc_error(const char* msg) { snprintf(t_tc_err, sizeof t_tc_err, "%s", msg); }
+
 // 4-D map over an e4m3 cache [NB, P, Hkv, 256]: box = one d-half (128 B) x 1 head x P rows
 // x 1 page, 128-byte swizzle.
 bool make_cache_tmap(CUtensorMap* m, const pg_tensor* t, int P) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
-    snprintf(t_tc_err, sizeof t_tc_err, "cuTensorMapEncodeTiled unavailable");
+    set_tc_error("cuTensorMapEncodeTiled unavailable");
     return false;
   }
   cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1], (cuuint64_t)t->shape[0]};
