@@ -83,7 +83,7 @@ int device_state(int dev, DeviceState** out) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct ClassSizes {
-  int num_ctas, max_blocks, max_items, max_slots;
+  int num_ctas, max_blocks, max_items, max_slots, slot_rows;
 };
 
 struct WsLayout {
@@ -98,23 +98,29 @@ WsLayout make_layout(int num_seqs, int T, int Hq, int Hkv, int sms) {
   const long long rows_all = (long long)T * G;
   // verify blocks: one per (sequence, kv head); prefill blocks: 128-row blocks
   const long long vb = (long long)num_seqs * Hkv;
-  const long long pb = (long long)Hkv * ((rows_all + kPrefillRows - 1) / kPrefillRows + num_seqs);
+  // a prefill block needs some sequence with q_len*G > 64, so none exist if T*G <= 64
+  const long long pb =
+      rows_all > kVerifyRows ? (long long)Hkv * ((rows_all + kPrefillRows - 1) / kPrefillRows + num_seqs) : 0;
   const long long nb[2] = {vb, pb};
+  const int rows[2] = {kVerifyRows, kPrefillRows};
   size_t at = 0;
   for (int c = 0; c < kNumClasses; ++c) {
     ClassSizes& s = L.cls[c];
     s.num_ctas = sms;
     s.max_blocks = (int)std::max<long long>(1, nb[c]);
     s.max_items = s.max_blocks + s.num_ctas;
-    s.max_slots = 2 * s.num_ctas;
+    // Split pieces: at most two per CTA range, and at most one per block plus one per
+    // CTA boundary that falls inside a block.
+    s.max_slots = nb[c] == 0 ? 0 : (int)std::min<long long>(2LL * s.num_ctas, nb[c] + s.num_ctas - 1);
+    s.slot_rows = rows[c];
     size_t sz[8] = {
-        256,                                                        // n_blocks, n_items, total_tiles
-        sizeof(int) * (size_t)(s.num_ctas + 1),                     // cta_item_begin
-        sizeof(RowBlock) * (size_t)s.max_blocks,                    // blocks
-        sizeof(WorkItem) * (size_t)s.max_items,                     // items
-        sizeof(int) * (size_t)s.max_blocks,                         // counters
-        sizeof(float) * (size_t)s.max_slots * kSlotRows * kHeadDim, // part_o
-        sizeof(float) * (size_t)s.max_slots * kSlotRows,            // part_lse
+        256,                                                          // n_blocks, n_items, total_tiles
+        sizeof(int) * (size_t)(s.num_ctas + 1),                       // cta_item_begin
+        sizeof(RowBlock) * (size_t)s.max_blocks,                      // blocks
+        sizeof(WorkItem) * (size_t)s.max_items,                       // items
+        sizeof(int) * (size_t)s.max_blocks,                           // counters
+        sizeof(float) * (size_t)s.max_slots * s.slot_rows * kHeadDim, // part_o
+        sizeof(float) * (size_t)s.max_slots * s.slot_rows,            // part_lse
         0};
     for (int i = 0; i < 8; ++i) {
       L.off[c][i] = at;
@@ -141,6 +147,7 @@ ClassPlan class_plan(const WsLayout& L, int c, char* base) {
   cp.max_blocks = L.cls[c].max_blocks;
   cp.max_items = L.cls[c].max_items;
   cp.max_slots = L.cls[c].max_slots;
+  cp.slot_rows = L.cls[c].slot_rows;
   return cp;
 }
 

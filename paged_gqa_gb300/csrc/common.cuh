@@ -83,10 +83,11 @@ struct ClassPlan {
   RowBlock* blocks;        // [max_blocks]
   WorkItem* items;         // [max_items]
   int* counters;           // [max_blocks]
-  float* part_o;           // [max_slots][kSlotRows][kHeadDim]
-  float* part_lse;         // [max_slots][kSlotRows] (log2 units)
+  float* part_o;           // [max_slots][slot_rows][kHeadDim]
+  float* part_lse;         // [max_slots][slot_rows] (log2 units)
   int num_ctas;
   int max_blocks, max_items, max_slots;
+  int slot_rows;           // rows of a block of this class (64 verify, 128 prefill)
 };
 
 }  // namespace pgqa

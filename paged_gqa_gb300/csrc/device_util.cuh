@@ -42,10 +42,10 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
 
 // Partial result slot of (block, split).
 __device__ __forceinline__ float* slot_o(const ClassPlan& cp, int slot) {
-  return cp.part_o + (size_t)slot * kSlotRows * kHeadDim;
+  return cp.part_o + (size_t)slot * cp.slot_rows * kHeadDim;
 }
 __device__ __forceinline__ float* slot_lse(const ClassPlan& cp, int slot) {
-  return cp.part_lse + (size_t)slot * kSlotRows;
+  return cp.part_lse + (size_t)slot * cp.slot_rows;
 }
 
 constexpr int kMergeMaxSplits = 16;  // pieces whose weights fit the shared scratch
