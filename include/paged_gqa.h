@@ -124,6 +124,26 @@ int paged_gqa_attn_ex(const pg_tensor* q, const pg_tensor* k_cache, const pg_ten
                       void* workspace, size_t workspace_bytes, pg_stream_t stream);
 
 /*
+ * paged_gqa_attn_noalloc -- the same call as paged_gqa_attn, for callers that cannot
+ * allocate device memory when they run attention (code inside an allocator or memory-pool
+ * callback, runtimes that fix their device footprint after start-up). The pages have no
+ * counterpart of this entry point.
+ *
+ * Arguments, layouts and results are those of paged_gqa_attn. Instead of a workspace it
+ * uses a 64 MiB scratch array that is part of the library's device image: every GPU that
+ * loads the library holds those 64 MiB until the process exits. It allocates nothing.
+ * A call whose workspace need (paged_gqa_workspace_size) exceeds 64 MiB returns
+ * PG_ERR_WORKSPACE and launches nothing. All calls on a device share the array; each
+ * call clears what must start at zero, but calls that can overlap on the GPU (unordered
+ * streams) race on it. The first call on each device looks up the array's address with
+ * that device current: make it before any stream capture.
+ */
+int paged_gqa_attn_noalloc(const pg_tensor* q, const pg_tensor* k_cache, const pg_tensor* v_cache,
+                           const pg_tensor* block_table, const pg_tensor* seq_lens,
+                           const pg_tensor* query_start_loc, float k_descale, float v_descale,
+                           float softmax_scale, pg_tensor* out, pg_stream_t stream);
+
+/*
  * Workspace bytes for a call with these host-known sizes on `device`
  * (num_seqs, total query tokens T, heads, page size, block-table width W).
  * Returns 0 on invalid sizes.

@@ -15,7 +15,8 @@ STATUS_NAMES = {0: "PG_OK", -1: "PG_ERR_INVALID_ARG", -2: "PG_ERR_UNSUPPORTED", 
                 -4: "PG_ERR_TIMEOUT", -5: "PG_ERR_DEVICE_BOUNDS", -6: "PG_ERR_WORKSPACE"}
 
 # Every symbol include/paged_gqa.h declares.
-EXPORTED = ("paged_gqa_attn", "paged_gqa_attn_ex", "paged_gqa_workspace_size", "paged_gqa_last_error",
+EXPORTED = ("paged_gqa_attn", "paged_gqa_attn_ex", "paged_gqa_attn_noalloc", "paged_gqa_workspace_size",
+            "paged_gqa_last_error",
             "paged_gqa_check_device_errors", "paged_gqa_set_path", "paged_gqa_last_plan",
             "paged_gqa_set_kernel_events", "paged_gqa_version")
 

@@ -22,6 +22,7 @@
 
 namespace pgqa {
 __device__ uint32_t g_error_word;
+int report_error(int code, const char* what, cudaError_t e);
 }
 
 using namespace pgqa;
@@ -355,6 +356,12 @@ int attn_common(const pg_tensor* q, const pg_tensor* k, const pg_tensor* v, cons
 }
 
 }  // namespace
+
+// Sets the calling thread's last-error message for a failed CUDA call; used by the
+// no-alloc entry point (noalloc.cu).
+int pgqa::report_error(int code, const char* what, cudaError_t e) {
+  return fail(code, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
 
 extern "C" {
 
