@@ -1,8 +1,8 @@
 // tc_util.cuh -- inline-PTX wrappers for sm_103a: mbarriers, TMA, tcgen05 (MMA, TMEM).
 //
-// Every wait is bounded: after kSpinLimit failed polls it records kErrTimeout in the
-// device error word, raises the CTA's abort flag and returns false, so no kernel can
-// hang the GPU on a lost arrival.
+// Every wait is bounded: after kWaitLimitNs of failed polls (global timer) it records
+// kErrTimeout in the device error word, raises the CTA's abort flag and returns false, so
+// no kernel can hang the GPU on a lost arrival.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -11,7 +11,13 @@
 namespace pgqa {
 namespace tc {
 
-constexpr uint32_t kSpinLimit = 1u << 25;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -42,9 +48,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity to complete.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t* err) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && *abort_flag) return false;
+    if ((i & 63u) == 0u) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) break;
+    }
   }
   atomicOr(err, kErrTimeout);
   *abort_flag = 1;
