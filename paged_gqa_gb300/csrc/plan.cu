@@ -96,6 +96,9 @@ plan_kernel(Problem p, Pointers ptr, ClassPlan c0, ClassPlan c1) {
   __shared__ long long s_total;
   __shared__ int s_overflow;
   ClassPlan plans[2] = {c0, c1};
+  // The attention kernels are launched as programmatic dependents: let them start their
+  // prologue now; they wait for this grid's completion before reading the plan.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     s_overflow = 0;
     if (p.num_seqs > 0 && (ptr.qsl[0] != 0 || ptr.qsl[p.num_seqs] != p.T)) atomicOr(ptr.err, kErrBounds);
@@ -120,28 +123,39 @@ plan_kernel(Problem p, Pointers ptr, ClassPlan c0, ClassPlan c1) {
     long long base = 0;
     for (int s0 = 0; s0 < p.num_seqs; s0 += blockDim.x) {
       int s = s0 + threadIdx.x;
-      SeqInfo si;
+      SeqInfo si = {0, 0, 0, 0};
       int nb = 0;
       if (s < p.num_seqs) {
         si = seq_info(p, ptr, s);
         nb = blocks_per_head(si, p.G, cls) * p.Hkv;
       }
       long long pre = block_exclusive_scan(nb, &s_total) + base;
-      if (s < p.num_seqs && nb > 0) {
-        const int per_head = nb / p.Hkv;
-        const int rows_total = si.qn * p.G;
-        const int rb_rows = cls == 0 ? kVerifyRows : kPrefillRows;
-        for (int i = 0; i < nb; ++i) {
-          long long bi = pre + i;
-          if (bi >= cp.max_blocks) { s_overflow = 1; break; }
+      // The warp fills the blocks of its 32 sequences together: one lane per block.
+      const int rb_rows = cls == 0 ? kVerifyRows : kPrefillRows;
+      const int lane = threadIdx.x & 31;
+      for (int j = 0; j < 32; ++j) {
+        const int nb_j = __shfl_sync(0xffffffffu, nb, j);
+        if (nb_j == 0) continue;
+        const long long pre_j = __shfl_sync(0xffffffffu, pre, j);
+        const int qn_j = __shfl_sync(0xffffffffu, si.qn, j);
+        const int L_j = __shfl_sync(0xffffffffu, si.L, j);
+        const int s_j = s0 + (threadIdx.x & ~31) + j;
+        const int per_head = nb_j / p.Hkv;
+        const int rows_total = qn_j * p.G;
+        for (int i = lane; i < nb_j; i += 32) {
+          const long long bi = pre_j + i;
+          if (bi >= cp.max_blocks) {
+            s_overflow = 1;
+            break;
+          }
           const int kvh = i / per_head, rb = i % per_head;
           RowBlock b;
-          b.seq = s;
+          b.seq = s_j;
           b.kvh = kvh;
           b.row0 = rb * rb_rows;
           b.nrows = min(rb_rows, rows_total - b.row0);
           const int t_last = (b.row0 + b.nrows - 1) / p.G;
-          b.kv_end = si.L - si.qn + t_last + 1;
+          b.kv_end = L_j - qn_j + t_last + 1;
           b.tiles = (b.kv_end + kTileKeys - 1) / kTileKeys;
           b.tile_off = 0;
           b.nsplit = 1;

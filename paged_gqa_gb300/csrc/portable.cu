@@ -15,6 +15,7 @@
 #include "common.cuh"
 #include "device_util.cuh"
 #include "plan.cuh"
+#include "tc_kernels.cuh"
 
 namespace pgqa {
 
@@ -90,8 +91,10 @@ portable_attn_kernel(Problem p, Pointers ptr, ClassPlan cp) {
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tq = lane & 3;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the plan kernel has completed
   const int item_begin = cp.cta_item_begin[blockIdx.x];
   const int item_end = cp.cta_item_begin[blockIdx.x + 1];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const size_t esz_q = p.q_is_fp8 ? 1 : 2, esz_kv = p.kv_is_fp8 ? 1 : 2;
 
   for (int it = item_begin; it < item_end; ++it) {
@@ -289,8 +292,8 @@ cudaError_t launch_portable(const Problem& p, const Pointers& ptr, const ClassPl
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  portable_attn_kernel<<<cp.num_ctas, kPThreads, kPSmemBytes, stream>>>(p, ptr, cp);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(portable_attn_kernel, cp.num_ctas, kPThreads, kPSmemBytes, stream, p, ptr, cp);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace pgqa

@@ -153,8 +153,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   Misc& ms = *reinterpret_cast<Misc*>(smem + LY::kOffMisc);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item_begin = cp.cta_item_begin[blockIdx.x];
-  const int item_end = cp.cta_item_begin[blockIdx.x + 1];
   volatile int* abort_flag = &ms.abort_flag;
   auto bar = [&](const uint64_t& b) { return smem_u32(&b); };
 
@@ -189,6 +187,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
+  // Launched as a programmatic dependent: the prologue above overlaps the previous
+  // kernel; the plan is read only after the previous grids have completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int item_begin = cp.cta_item_begin[blockIdx.x];
+  const int item_end = cp.cta_item_begin[blockIdx.x + 1];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0 || warp == kVProducerWarp) {
     // ------------------------------------------------------------ TMA producers (K, V)
@@ -433,10 +437,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       const int min_lim = I.L - I.qn + map_row(I.row0, p.G, I.kvh).t;
       m_ref = kMInit;
       l = 0.f;
-      bool aborted = false;
-      for (int j = 0; j < I.ntiles; ++j, ++g) {
+      const int kv_hi = I.kv_hi, tile_begin = I.tile_begin, ntiles = I.ntiles;
+      const int hi_key = min(kv_hi - 1, lim);  // keys <= hi_key are visible to this row
+      const bool c_pos = c >= 0.f;
+      // A failed wait (timeout or abort) does not leave the loop: every later wait then
+      // fails fast, so all softmax warps still pass the same barriers and finish.
+      for (int j = 0; j < ntiles; ++j, ++g) {
         const int b = g & 1;
-        const int key0 = (I.tile_begin + j) * kTileKeys;
+        const int key0 = (tile_begin + j) * kTileKeys;
         const int kbase = key0 + kh * kHalfKeys;
         float t[kHalfKeys];
         if (!mbar_wait(bar(ms.s_full[b]), (g >> 1) & 1, abort_flag, ptr.err)) bad = true;
@@ -451,36 +459,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(ms.s_free[b]));
+        // masked tiles hold scaled scores; unmasked tiles keep raw scores and take the
+        // scale in the exponent's FFMA
+        const bool need_mask = (key0 + kTileKeys > kv_hi) || (key0 + kTileKeys - 1 > min_lim);
         float mx = -INFINITY;
-        const bool need_mask = (key0 + kTileKeys > I.kv_hi) || (key0 + kTileKeys - 1 > min_lim);
         if (need_mask) {
-          const int hi_key = min(I.kv_hi - 1, lim);  // keys <= hi_key are visible to this row
 #pragma unroll
           for (int i = 0; i < kHalfKeys; ++i) {
             t[i] = (kbase + i <= hi_key) ? t[i] * c : -INFINITY;
             mx = fmaxf(mx, t[i]);
           }
+        } else if (c_pos) {
+#pragma unroll
+          for (int i = 0; i < kHalfKeys; ++i) mx = fmaxf(mx, t[i]);
+          mx *= c;
         } else {
 #pragma unroll
-          for (int i = 0; i < kHalfKeys; ++i) {
-            t[i] *= c;
-            mx = fmaxf(mx, t[i]);
-          }
+          for (int i = 0; i < kHalfKeys; ++i) mx = fmaxf(mx, -t[i]);
+          mx *= -c;
         }
-        // the row's maximum over both key halves (partner thread: same lane, other warp)
+        // the row's maximum over both key halves (partner: same lane, the other warp)
         ms.red[g & 1][kh][row] = mx;
-        // abort vote rides on the same exchange: any warp of the group that saw a failed
-        // wait makes every warp leave at this tile
-        const int wv = (bad || *abort_flag) ? 2 : 0;
-        if (lane == 0) ms.vote[g & 1][sw] = wv;
-        named_barrier(9, kSoftThreads);
-        int votes = 0;
-#pragma unroll
-        for (int w = 0; w < kSoftWarps; ++w) votes |= ms.vote[g & 1][w];
-        if (votes & 2) {
-          aborted = true;
-          break;
-        }
+        named_barrier(pair_bar, 64);
         const float mt = fmaxf(mx, ms.red[g & 1][kh ^ 1][row]);
         float alpha = 1.f;
         const bool rescale = mt > m_ref + kTau;
@@ -489,18 +489,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           m_ref = mt;
           l *= alpha;
         }
-        // P = 2^(t - m + sigma) -> e4m3 hi + lo, 4 keys per word
+        // P = 2^(s c - m + sigma) in f16, split into e4m3 hi + lo, 4 keys per word
         uint32_t ph[kHalfKeys / 4], pl[kHalfKeys / 4];
-        float ps = 0.f;
         const float off = m_ref - kSigma;
+        const float sc = need_mask ? 1.f : c;
+        __half2 acc[4] = {__float2half2_rn(0.f), __float2half2_rn(0.f), __float2half2_rn(0.f),
+                          __float2half2_rn(0.f)};
 #pragma unroll
         for (int i = 0; i < kHalfKeys; i += 4) {
-          const float p0 = ex2(t[i] - off), p1 = ex2(t[i + 1] - off);
-          const float p2 = ex2(t[i + 2] - off), p3 = ex2(t[i + 3] - off);
-          ps += (p0 + p1) + (p2 + p3);
-          split4(p0, p1, p2, p3, ph[i / 4], pl[i / 4]);
+          __half2 s01, s23;
+          p_split4_f16(fmaf(t[i], sc, -off), fmaf(t[i + 1], sc, -off), fmaf(t[i + 2], sc, -off),
+                       fmaf(t[i + 3], sc, -off), ph[i / 4], pl[i / 4], s01, s23);
+          acc[(i / 4) & 3] = __hadd2(acc[(i / 4) & 3], __hadd2(s01, s23));
         }
-        l += ps;
+        const float2 ls = __half22float2(__hadd2(__hadd2(acc[0], acc[1]), __hadd2(acc[2], acc[3])));
+        l += ls.x + ls.y;
         if (g >= 1 && !mbar_wait(bar(ms.p_free), (g - 1) & 1, abort_flag, ptr.err)) bad = true;
         tc_fence_after();
         // tcgen05.ld/st are warp-collective: a warp rescales if any of its rows must,
@@ -520,12 +523,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           }
           tmem_wait_st();
         }
-        if (key0 + kTileKeys > I.kv_hi) {
+        if (key0 + kTileKeys > kv_hi) {
           // keys past the piece's end: their V rows (stale or NaN slots) become zeros.
           // thread (kh, row) zeroes d-half kh of key `row`
           const uint32_t st = g % kVStages;
           if (!mbar_wait(bar(ms.v_full[st]), (g / kVStages) & 1, abort_flag, ptr.err)) bad = true;
-          if (key0 + row >= I.kv_hi) {
+          if (key0 + row >= kv_hi) {
             const uint4 z = make_uint4(0, 0, 0, 0);
             uint4* dst = reinterpret_cast<uint4*>(smem + LY::kOffV + st * kKVTile + kh * kKVHalf + row * 128);
 #pragma unroll
@@ -546,7 +549,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         tc_fence_before();
         mbar_arrive(bar(ms.p_full));
       }
-      if (aborted) break;
       if (it + 1 < item_end) q_prep(load_item(cp, ptr, it + 1), ii + 1);
 
       // ---------------------------------------------------------- epilogue
@@ -632,8 +634,8 @@ int launch_prefill_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp
     }
     attr_done[dev] |= which;
   }
-  kern<<<cp.num_ctas, kThreads, bytes, stream>>>(tk, tv, p, ptr, cp);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, cp.num_ctas, kThreads, bytes, stream, tk, tv, p, ptr, cp);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     char buf[160];
     snprintf(buf, sizeof buf, "prefill kernel launch: %s", cudaGetErrorString(e));

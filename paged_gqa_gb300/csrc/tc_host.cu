@@ -1,0 +1,70 @@
+// tc_host.cu -- host helpers of the tcgen05 kernels: TMA tensor maps over the paged caches
+// and the launch-error message.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "tc_kernels.cuh"
+
+namespace pgqa {
+
+namespace {
+
+std::mutex g_tc_mu;
+thread_local char t_tc_err[256] = "";
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link to libcuda).
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  std::lock_guard<std::mutex> lk(g_tc_mu);
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+}  // namespace
+
+void set_tc_error(const char* msg) { snprintf(t_tc_err, sizeof t_tc_err, "%s", msg); }
+
+const char* tc_last_error() { return t_tc_err; }
+
+// 4-D map over an e4m3 cache [NB, P, Hkv, 256]: box = one d-half (128 B) x 1 head x P rows
+// x 1 page, 128-byte swizzle, so one box lands a page's half-rows in the layout the MMA
+// descriptors expect (8-row atoms of 128 B).
+bool make_cache_tmap(CUtensorMap* m, const pg_tensor* t, int P) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    set_tc_error("cuTensorMapEncodeTiled unavailable");
+    return false;
+  }
+  cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1],
+                        (cuuint64_t)t->shape[0]};
+  cuuint64_t strides[3] = {(cuuint64_t)t->stride[2], (cuuint64_t)t->stride[1], (cuuint64_t)t->stride[0]};
+  cuuint32_t box[4] = {128, 1, (cuuint32_t)P, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, t->data, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[96];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    set_tc_error(buf);
+    return false;
+  }
+  return true;
+}
+
+}  // namespace pgqa

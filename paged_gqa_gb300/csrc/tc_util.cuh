@@ -183,6 +183,30 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// x0..x3 (exponents, <= 8) -> p = 2^x in f16, then p = hi + lo with hi, lo in e4m3:
+// hi/lo get one byte per key (x0 in the low byte), s01/s23 the f16 values of p.
+__device__ __forceinline__ void p_split4_f16(float x0, float x1, float x2, float x3, uint32_t& hi, uint32_t& lo,
+                                             __half2& s01, __half2& s23) {
+  uint32_t a, b, ha, hb, ba, bb, ra, rb;
+  uint16_t ea, eb, la, lb;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(a) : "f"(x1), "f"(x0));
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(b) : "f"(x3), "f"(x2));
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(ha) : "r"(a));
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(hb) : "r"(b));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(ea) : "r"(ha));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(eb) : "r"(hb));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(ba) : "h"(ea));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(bb) : "h"(eb));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(ra) : "r"(ha), "r"(ba));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(rb) : "r"(hb), "r"(bb));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(la) : "r"(ra));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(lb) : "r"(rb));
+  hi = (uint32_t)ea | ((uint32_t)eb << 16);
+  lo = (uint32_t)la | ((uint32_t)lb << 16);
+  s01 = *reinterpret_cast<__half2*>(&ha);
+  s23 = *reinterpret_cast<__half2*>(&hb);
+}
+
 // Two e4m3 codes (low byte first) -> two exact floats.
 __device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t v) {
   uint32_t h2;

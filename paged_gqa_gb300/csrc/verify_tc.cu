@@ -7,16 +7,18 @@
 // the FP8 descales are per-tensor scalars. The launch shape on that page (BLOCK_M 32,
 // TILE 32, 8-64 segments on gfx950) is prior art; this kernel is laid out for sm_103a:
 //
-//   * swap-AB: the 128 keys of a tile are the MMA's M dimension and the (padded) 64 query
-//     rows are N, so a 64-row verify block fills the 128-lane tensor core. S^T = K Q^T and
-//     O^T += V^T P^T, both tcgen05.mma kind::f8f6f4 with fp32 accumulators in TMEM;
+//   * swap-AB: the 128 keys of a tile are the MMA's M dimension and the query rows are N,
+//     so a short query still fills the 128-lane tensor core;
 //   * FP8 K and V go from HBM to shared memory by TMA (one box per page and d-half,
-//     addressed through the block table) and into the MMA untouched; the dequant scales are
-//     folded into the score scale (k_descale) and the output scale (v_descale);
+//     addressed through the block table) and into tcgen05.mma kind::f8f6f4 untouched; the
+//     dequant scales are folded into the score scale (k_descale) and the output scale
+//     (v_descale);
 //   * bf16 Q is split once per block into e4m3 hi + lo parts (q*2^s = hi + lo, exact to
-//     ~2^-16 of the block's max), so S = K.hi + K.lo costs two FP8 MMAs and no K conversion;
-//   * P is split the same way (p = hi + lo in e4m3, ~9 significant bits, about bf16's
-//     precision); a single e4m3 P would miss the 5e-3 relative-L2 bar;
+//     ~2^-16 of the block's max); both parts are stacked as one N = 128 operand, so
+//     [S_hi | S_lo] = K [Q_hi; Q_lo]^T is 8 MMAs that read each K tile once;
+//   * P is split the same way (p = hi + lo in e4m3, about bf16's precision; a single e4m3
+//     P would miss the 5e-3 relative-L2 bar) and stacked the same way, so
+//     [O_hi | O_lo] = V^T [P_hi; P_lo]^T is 8 MMAs that read each V tile once; O = O_hi + O_lo;
 //   * online softmax over keys: keys live on TMEM lanes, so the row max is a cross-lane
 //     reduction (redux.sync + shared memory). It is only taken when some score exceeds the
 //     running reference by 2^4 (the reference then moves to the exact max and O^T and the
@@ -28,15 +30,14 @@
 // warps 2-9 = softmax and epilogue, warp 10 = V producer (TMA). Softmax thread (q, c, lane)
 // owns TMEM lane 32q+lane (= key of the tile, = d within a d-half for O^T) and rows
 // [32c, 32c+32). Shared memory: Q hi/lo 32 KB, 2 K stages and 3 V stages of 32 KB, P hi/lo
-// 16 KB, barriers and row state (~221 KB, one CTA per SM).
+// 16 KB, barriers and row state (~221 KB, one CTA per SM). TMEM: 2 S buffers of 128
+// columns, O^T 256 columns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
 #include <cstdio>
-#include <cstring>
-#include <mutex>
 
 #include "common.cuh"
 #include "device_util.cuh"
@@ -49,7 +50,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kVN = 64;            // MMA N: query rows, padded
+constexpr int kVN = 64;            // query rows of a verify block (MMA N per Q or P part)
 constexpr int kSoftWarps = 8;
 constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kVThreads = 96 + kSoftThreads;  // + K producer, MMA, V producer warps
@@ -61,33 +62,34 @@ constexpr float kTau = 4.f;        // rescale when a score exceeds the reference
 constexpr float kSigma = 4.f;      // P is stored scaled by 2^kSigma (max 2^(kTau+kSigma) = 256)
 constexpr float kMInit = -1.0e30f; // reference of a row before its first key
 
-constexpr uint32_t kQHalf = kVN * 128;          // [64 rows][128 B] e4m3, one d-half
-constexpr uint32_t kQPart = 2 * kQHalf;
+// Q: per d-half h, [Q_hi 64 rows][Q_lo 64 rows] x 128 B (K-major, 128B swizzle).
+constexpr uint32_t kQHalf = 2 * kVN * 128;      // 16 KB
+constexpr uint32_t kQPartOff = kVN * 128;       // Q_lo rows start 8 KB into the half
 constexpr uint32_t kKVHalf = kTileKeys * 128;   // [128 keys][128 B]
 constexpr uint32_t kKVTile = 2 * kKVHalf;
-constexpr uint32_t kPPart = kTileKeys * kVN;    // [128 keys][64 B]
-constexpr uint32_t kOffQhi = 0;
-constexpr uint32_t kOffQlo = kOffQhi + kQPart;
-constexpr uint32_t kOffK = kOffQlo + kQPart;
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + 2 * kQHalf;
 constexpr uint32_t kOffV = kOffK + kKStages * kKVTile;
-constexpr uint32_t kOffPhi = kOffV + kVStages * kKVTile;
-constexpr uint32_t kOffPlo = kOffPhi + kPPart;
-constexpr uint32_t kOffMisc = kOffPlo + kPPart;
+constexpr uint32_t kOffP = kOffV + kVStages * kKVTile;  // [128 keys][P_hi 64 B | P_lo 64 B]
+constexpr uint32_t kOffMisc = kOffP + kTileKeys * 128;
 
-// TMEM columns: S^T double buffer, then O^T (d-half 0, d-half 1).
-constexpr uint32_t kTmemCols = 256;
+// TMEM columns: S buffers [S_hi | S_lo] (2 x 128), O^T d-half h [O_hi | O_lo] (2 x 128).
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 128;
+constexpr uint32_t kColO = 256;
 
-constexpr uint32_t kIdescS = idesc_e4m3(128, kVN, false, false);  // K (K-major) x Q^T (K-major)
-constexpr uint32_t kIdescO = idesc_e4m3(128, kVN, true, true);    // V^T (MN-major) x P^T (MN-major)
+template <bool kQFp8>
+struct Shapes {
+  static constexpr int kSN = kQFp8 ? kVN : 2 * kVN;  // S MMA N: Q, or [Q_hi; Q_lo]
+};
+constexpr uint32_t kIdescO = idesc_e4m3(128, 2 * kVN, true, true);  // V^T (MN) x [P_hi; P_lo]^T (MN)
 
 struct Misc {
   // arrays read with 16-byte vector loads first
   alignas(16) float m[2][kVN];
+  alignas(16) float mo[2][kVN];   // kSigma - m: the per-row offset of the exponent
   alignas(16) float red[4][kVN];
   alignas(16) float alpha[kVN];
-  alignas(16) float lrow[kVN];
   alignas(16) int lim[2][kVN];
   alignas(16) long long out_off[2][kVN];
   alignas(16) float merge_w[kMergeMaxSplits * kSlotRows];
@@ -152,13 +154,13 @@ template <bool kQFp8>
 __global__ void __launch_bounds__(kVThreads, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  Problem p, Pointers ptr, ClassPlan cp) {
+  constexpr int kSN = Shapes<kQFp8>::kSN;
+  constexpr uint32_t kIdescS = idesc_e4m3(128, kSN, false, false);  // K (K-major) x Q (K-major)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Misc& ms = *reinterpret_cast<Misc*>(smem + kOffMisc);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item_begin = cp.cta_item_begin[blockIdx.x];
-  const int item_end = cp.cta_item_begin[blockIdx.x + 1];
   volatile int* abort_flag = &ms.abort_flag;
 
   auto bar = [&](const uint64_t& b) { return smem_u32(&b); };
@@ -194,6 +196,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
+  // When launched as a programmatic dependent of the plan kernel, the prologue above
+  // overlaps it; the plan is read only after it has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int item_begin = cp.cta_item_begin[blockIdx.x];
+  const int item_end = cp.cta_item_begin[blockIdx.x + 1];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0 || warp == kVProducerWarp) {
     // ------------------------------------------------------------ TMA producers (K, V)
@@ -285,12 +293,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         if (!mbar_wait(bar(ms.v_full[st]), (t.g / kVStages) & 1, abort_flag, ptr.err)) return false;
         tc_fence_after();
         for (int h = 0; h < 2; ++h) {
-          for (int part = 0; part < 2; ++part) {
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = smem_desc(sbase + kOffV + st * kKVTile + h * kKVHalf + kk * 4096, 1024, 1024, kSw128);
-              const uint64_t b = smem_desc(sbase + (part ? kOffPlo : kOffPhi) + kk * 2048, 512, 512, kSw64);
-              mma_e4m3(tmem + kColO + h * kVN, a, b, kIdescO, (t.first && part == 0 && kk == 0) ? 0u : 1u);
-            }
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t a = smem_desc(sbase + kOffV + st * kKVTile + h * kKVHalf + kk * 4096, 1024, 1024, kSw128);
+            const uint64_t b = smem_desc(sbase + kOffP + kk * 4096, 1024, 1024, kSw128);
+            mma_e4m3(tmem + kColO + h * 128, a, b, kIdescO, (t.first && kk == 0) ? 0u : 1u);
           }
         }
         mma_commit(bar(ms.v_empty[st]));
@@ -306,14 +312,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           if (!(ok = mbar_wait(bar(ms.k_full[st]), (g / kKStages) & 1, abort_flag, ptr.err))) break;
           if (g >= 2 && !(ok = mbar_wait(bar(ms.s_free[b]), ((g >> 1) - 1) & 1, abort_flag, ptr.err))) break;
           tc_fence_after();
-          const int parts = kQFp8 ? 1 : 2;
-          for (int part = 0; part < parts; ++part) {
-            for (int kb = 0; kb < 8; ++kb) {
-              const int h = kb >> 2, kk = kb & 3;
-              const uint64_t a = smem_desc(sbase + kOffK + st * kKVTile + h * kKVHalf + kk * 32, 16, 1024, kSw128);
-              const uint64_t bq = smem_desc(sbase + (part ? kOffQlo : kOffQhi) + h * kQHalf + kk * 32, 16, 1024, kSw128);
-              mma_e4m3(tmem + kColS + b * kVN, a, bq, kIdescS, (part | kb) ? 1u : 0u);
-            }
+          for (int kb = 0; kb < 8; ++kb) {
+            const int h = kb >> 2, kk = kb & 3;
+            const uint64_t a = smem_desc(sbase + kOffK + st * kKVTile + h * kKVHalf + kk * 32, 16, 1024, kSw128);
+            const uint64_t bq = smem_desc(sbase + kOffQ + h * kQHalf + kk * 32, 16, 1024, kSw128);
+            mma_e4m3(tmem + kColS + b * 128, a, bq, kIdescS, kb ? 1u : 0u);
           }
           mma_commit(bar(ms.s_full[b]));
           mma_commit(bar(ms.k_empty[st]));
@@ -356,6 +359,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
         // padding rows: a finite reference, so their (discarded) scores never vote
         ms.m[pi][n] = n < I.nrows ? kMInit : 0.f;
+        ms.mo[pi][n] = kSigma - ms.m[pi][n];
       }
       // 64 rows x 16 chunks of 16 elements; thread gi takes chunks gi + 256k, k < 4
       auto src_of = [&](int r, int ch) -> const uint8_t* {
@@ -363,9 +367,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         return static_cast<const uint8_t*>(ptr.q) +
                ((size_t)(I.q0 + m.t) * p.q_st + (size_t)m.h * p.q_sh + ch * 16) * (kQFp8 ? 1 : 2);
       };
-      auto dst_of = [&](uint32_t part_off, int r, int ch) -> uint8_t* {
-        const int h = ch >> 3, c = ch & 7;
-        return smem + part_off + h * kQHalf + r * 128 + ((c ^ (r & 7)) << 4);
+      // part 0 = hi rows 0..63, part 1 = lo rows 64..127 of the stacked operand
+      auto dst_of = [&](int part, int r, int ch) -> uint8_t* {
+        const int h = ch >> 3, c = ch & 7, rr = part * kVN + r;
+        return smem + kOffQ + h * kQHalf + rr * 128 + ((c ^ (rr & 7)) << 4);
       };
       if (kQFp8) {
         uint4 v[4];
@@ -377,7 +382,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int c = gi + k * kSoftThreads, r = c >> 4, ch = c & 15;
-          *reinterpret_cast<uint4*>(dst_of(kOffQhi, r, ch)) = v[k];
+          *reinterpret_cast<uint4*>(dst_of(0, r, ch)) = v[k];
         }
         if (gi == 0) ms.qscale[pi] = 1.f;
       } else {
@@ -426,13 +431,29 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             const float2 f0 = bf2(w[2 * i]), f1 = bf2(w[2 * i + 1]);
             split4(f0.x * scale, f0.y * scale, f1.x * scale, f1.y * scale, hw[i], lw[i]);
           }
-          *reinterpret_cast<uint4*>(dst_of(kOffQhi, r, ch)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(dst_of(kOffQlo, r, ch)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          *reinterpret_cast<uint4*>(dst_of(0, r, ch)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(dst_of(1, r, ch)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
         if (gi == 0) ms.qscale[pi] = ldexpf(1.f, -sig);
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(ms.q_full));
+    };
+
+    // scores of this thread's key for its 32 rows: S_hi + S_lo (one part for FP8 Q)
+    auto load_s = [&](int b, float (&t)[kCols]) {
+#pragma unroll
+      for (int k = 0; k < kCols; k += 16) {
+        float v[16];
+        tmem_ld16(tmem + lane_addr + kColS + b * 128 + c0 + k, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) t[k + i] = v[i];
+        if (!kQFp8) {
+          tmem_ld16(tmem + lane_addr + kColS + b * 128 + kVN + c0 + k, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) t[k + i] += v[i];
+        }
+      }
     };
 
     int ii = 0;
@@ -452,36 +473,38 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         float t[kCols];
         if (!mbar_wait(bar(ms.s_full[b]), (g >> 1) & 1, abort_flag, ptr.err)) bad = true;
         tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < kCols; k += 16) {
-          float v[16];
-          tmem_ld16(tmem + lane_addr + kColS + b * kVN + c0 + k, v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) t[k + i] = v[i];
-        }
+        load_s(b, t);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(ms.s_free[b]));
+        // x = s c - m + sigma: the exponent of P, one FFMA per score
         const bool need_mask = (key0 + kTileKeys > I.kv_hi) || (key0 + kTileKeys - 1 > min_lim);
+        float xmax = -INFINITY;
         if (need_mask) {
           const bool kin = key < I.kv_hi;
 #pragma unroll
-          for (int n = 0; n < kCols; ++n) {
-            const bool vis = kin && key <= ms.lim[pi][c0 + n];
-            t[n] = vis ? t[n] * c : -INFINITY;
+          for (int n = 0; n < kCols; n += 4) {
+            const float4 o4 = *reinterpret_cast<const float4*>(&ms.mo[pi][c0 + n]);
+            const int4 l4 = *reinterpret_cast<const int4*>(&ms.lim[pi][c0 + n]);
+            t[n] = (kin && key <= l4.x) ? fmaf(t[n], c, o4.x) : -INFINITY;
+            t[n + 1] = (kin && key <= l4.y) ? fmaf(t[n + 1], c, o4.y) : -INFINITY;
+            t[n + 2] = (kin && key <= l4.z) ? fmaf(t[n + 2], c, o4.z) : -INFINITY;
+            t[n + 3] = (kin && key <= l4.w) ? fmaf(t[n + 3], c, o4.w) : -INFINITY;
+            xmax = fmaxf(xmax, fmaxf(fmaxf(t[n], t[n + 1]), fmaxf(t[n + 2], t[n + 3])));
           }
         } else {
 #pragma unroll
-          for (int n = 0; n < kCols; ++n) t[n] = t[n] * c;
+          for (int n = 0; n < kCols; n += 4) {
+            const float4 o4 = *reinterpret_cast<const float4*>(&ms.mo[pi][c0 + n]);
+            t[n] = fmaf(t[n], c, o4.x);
+            t[n + 1] = fmaf(t[n + 1], c, o4.y);
+            t[n + 2] = fmaf(t[n + 2], c, o4.z);
+            t[n + 3] = fmaf(t[n + 3], c, o4.w);
+            xmax = fmaxf(xmax, fmaxf(fmaxf(t[n], t[n + 1]), fmaxf(t[n + 2], t[n + 3])));
+          }
         }
         // vote: does any score exceed its row reference by more than 2^kTau?
-        bool mine = false;
-#pragma unroll
-        for (int n = 0; n < kCols; n += 4) {
-          const float4 m4 = *reinterpret_cast<const float4*>(&ms.m[pi][c0 + n]);
-          mine |= (t[n] - m4.x > kTau) | (t[n + 1] - m4.y > kTau) | (t[n + 2] - m4.z > kTau) |
-                  (t[n + 3] - m4.w > kTau);
-        }
+        const bool mine = xmax > kTau + kSigma;
         const int wv = (__any_sync(0xffffffffu, mine) ? 1 : 0) | ((bad || *abort_flag) ? 2 : 0);
         if (lane == 0) ms.vote[g & 1][sw] = wv;
         named_barrier(1, kSoftThreads);
@@ -494,8 +517,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
         const bool rescale = votes & 1;
         if (rescale) {
+          // Reload the raw scores (S buffer b is only overwritten after this tile's P is
+          // published; x may have lost s entirely against a -1e30 reference), take the
+          // exact tile maximum of s c per row, then the new reference.
+          tc_fence_after();
+          load_s(b, t);
+          tmem_wait_ld();
+          const bool kin = key < I.kv_hi;
 #pragma unroll
           for (int n = 0; n < kCols; ++n) {
+            const bool vis = !need_mask || (kin && key <= ms.lim[pi][c0 + n]);
+            t[n] = vis ? t[n] * c : -INFINITY;  // s c, masked
             const float r = warp_max(t[n]);
             if (lane == n) ms.red[q4][c0 + n] = r;
           }
@@ -503,38 +535,42 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           if (gi < kVN) {
             const int n = gi;
             const float mt = fmaxf(fmaxf(ms.red[0][n], ms.red[1][n]), fmaxf(ms.red[2][n], ms.red[3][n]));
-            const float mo = ms.m[pi][n];
-            const float mn = fmaxf(mo, mt);
-            ms.alpha[n] = ex2(mo - mn);
+            const float m_old = ms.m[pi][n];
+            const float mn = fmaxf(m_old, mt);
+            ms.alpha[n] = ex2(m_old - mn);
             ms.m[pi][n] = mn;
+            ms.mo[pi][n] = kSigma - mn;
           }
           named_barrier(1, kSoftThreads);
 #pragma unroll
-          for (int n = 0; n < kCols; ++n) l[n] *= ms.alpha[c0 + n];
+          for (int n = 0; n < kCols; ++n) {
+            t[n] += ms.mo[pi][c0 + n];
+            l[n] *= ms.alpha[c0 + n];
+          }
         }
-        // P = 2^(t - m + sigma), split into e4m3 hi + lo, 4 rows per word
+        // P = 2^x in f16, split into e4m3 hi + lo (4 rows per word); row sums in fp32
         uint32_t ph[kCols / 4], pl[kCols / 4];
 #pragma unroll
         for (int n = 0; n < kCols; n += 4) {
-          const float4 m4 = *reinterpret_cast<const float4*>(&ms.m[pi][c0 + n]);
-          const float p0 = ex2(t[n] - m4.x + kSigma), p1 = ex2(t[n + 1] - m4.y + kSigma);
-          const float p2 = ex2(t[n + 2] - m4.z + kSigma), p3 = ex2(t[n + 3] - m4.w + kSigma);
-          l[n] += p0;
-          l[n + 1] += p1;
-          l[n + 2] += p2;
-          l[n + 3] += p3;
-          split4(p0, p1, p2, p3, ph[n / 4], pl[n / 4]);
+          __half2 s01, s23;
+          p_split4_f16(t[n], t[n + 1], t[n + 2], t[n + 3], ph[n / 4], pl[n / 4], s01, s23);
+          const float2 f01 = __half22float2(s01), f23 = __half22float2(s23);
+          l[n] += f01.x;
+          l[n + 1] += f01.y;
+          l[n + 2] += f23.x;
+          l[n + 3] += f23.y;
         }
         // P buffer and O^T are free once the previous tile's P.V has completed
         if (g >= 1 && !mbar_wait(bar(ms.p_free), (g - 1) & 1, abort_flag, ptr.err)) bad = true;
         tc_fence_after();
         if (rescale && j > 0) {
+          // O^T (both d-halves, both P parts), column by column
 #pragma unroll 1
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < 4; ++h) {
 #pragma unroll 1
             for (int k = 0; k < kCols; k += 16) {
               float v[16];
-              const uint32_t a = tmem + lane_addr + kColO + h * kVN + c0 + k;
+              const uint32_t a = tmem + lane_addr + kColO + (h >> 1) * 128 + (h & 1) * kVN + c0 + k;
               tmem_ld16(a, v);
               tmem_wait_ld();
 #pragma unroll
@@ -556,16 +592,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             for (int i = 0; i < 8; ++i) row[i] = z;
           }
         }
-        // P^T rows: key ti, rows [c0, c0+32) of each part, 64-byte swizzle
+        // P^T row of key ti: [P_hi rows 0..63 | P_lo rows 0..63], 128-byte swizzle; this
+        // thread writes rows [c0, c0+32) of both parts
         {
-          const int swz = (ti >> 1) & 3;
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
-            const int chunk = (c0 >> 4) + cc;
-            const uint32_t off = ti * 64 + ((chunk ^ swz) << 4);
-            *reinterpret_cast<uint4*>(smem + kOffPhi + off) =
+            const int chunk_hi = (c0 >> 4) + cc, chunk_lo = 4 + chunk_hi;
+            *reinterpret_cast<uint4*>(smem + kOffP + ti * 128 + ((chunk_hi ^ (ti & 7)) << 4)) =
                 make_uint4(ph[4 * cc], ph[4 * cc + 1], ph[4 * cc + 2], ph[4 * cc + 3]);
-            *reinterpret_cast<uint4*>(smem + kOffPlo + off) =
+            *reinterpret_cast<uint4*>(smem + kOffP + ti * 128 + ((chunk_lo ^ (ti & 7)) << 4)) =
                 make_uint4(pl[4 * cc], pl[4 * cc + 1], pl[4 * cc + 2], pl[4 * cc + 3]);
           }
         }
@@ -599,32 +634,37 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         ms.red[q4][c0 + lane] = v[0];
       }
       named_barrier(1, kSoftThreads);
-      if (gi < kVN) {
-        const int n = gi;
-        ms.lrow[n] = ms.red[0][n] + ms.red[1][n] + ms.red[2][n] + ms.red[3][n];
+      float inv[kCols];
+#pragma unroll
+      for (int n = 0; n < kCols; ++n) {
+        const float lr = ms.red[0][c0 + n] + ms.red[1][c0 + n] + ms.red[2][c0 + n] + ms.red[3][c0 + n];
+        inv[n] = lr > 0.f ? p.out_scale / lr : 0.f;
       }
-      named_barrier(1, kSoftThreads);
+      float my_l = 0.f;  // row c0 + lane, for the partial's log-sum-exp
+      if (q4 == 0) my_l = ms.red[0][c0 + lane] + ms.red[1][c0 + lane] + ms.red[2][c0 + lane] + ms.red[3][c0 + lane];
+      named_barrier(1, kSoftThreads);  // red is reused by the next item's first rescale
       const bool split = I.nsplit > 1;
       const int slot = I.slot_base + I.split;
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
-#pragma unroll 1
-        for (int k = 0; k < kCols; k += 16) {
-          if (c0 + k >= I.nrows) break;
-          float v[16];
-          tmem_ld16(tmem + lane_addr + kColO + h * kVN + c0 + k, v);
-          tmem_wait_ld();
-          const int d = h * 128 + ti;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int n = c0 + k + i;
-            if (n < I.nrows) {
-              const float lr = ms.lrow[n];
-              const float val = lr > 0.f ? v[i] * (p.out_scale / lr) : 0.f;
-              if (split) {
-                slot_o(cp, slot)[(size_t)n * kHeadDim + d] = val;
-              } else {
-                static_cast<__nv_bfloat16*>(ptr.out)[ms.out_off[pi][n] + d] = __float2bfloat16_rn(val);
+        for (int k = 0; k < kCols; k += 16) {
+          if (c0 + k < I.nrows) {  // warp-uniform
+            float v[16], w[16];
+            tmem_ld16(tmem + lane_addr + kColO + h * 128 + c0 + k, v);
+            tmem_ld16(tmem + lane_addr + kColO + h * 128 + kVN + c0 + k, w);
+            tmem_wait_ld();
+            const int d = h * 128 + ti;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int n = c0 + k + i;
+              if (n < I.nrows) {
+                const float val = (v[i] + w[i]) * inv[k + i];
+                if (split) {
+                  slot_o(cp, slot)[(size_t)n * kHeadDim + d] = val;
+                } else {
+                  static_cast<__nv_bfloat16*>(ptr.out)[ms.out_off[pi][n] + d] = __float2bfloat16_rn(val);
+                }
               }
             }
           }
@@ -633,9 +673,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       tc_fence_before();
       mbar_arrive(bar(ms.o_free));
       if (split) {
-        if (gi < I.nrows) {
-          const float lr = ms.lrow[gi];
-          slot_lse(cp, slot)[gi] = lr > 0.f ? ms.m[pi][gi] - kSigma + log2f(lr) : -INFINITY;
+        if (q4 == 0 && c0 + lane < I.nrows) {
+          const int row = c0 + lane;
+          slot_lse(cp, slot)[row] = my_l > 0.f ? ms.m[pi][row] - kSigma + log2f(my_l) : -INFINITY;
         }
         __threadfence();
         RowBlock rb;
@@ -660,59 +700,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   }
 }
 
-// ---------------------------------------------------------------- host side --
-
-namespace {
-
-std::mutex g_tc_mu;
-thread_local char t_tc_err[256] = "";
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  std::lock_guard<std::mutex> lk(g_tc_mu);
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  }
-  return fn;
-}
-
-}  // namespace
-
-void set_tc_error(const char* msg) { snprintf(t_tc_err, sizeof t_tc_err, "%s", msg); }
-
-// 4-D map over an e4m3 cache [NB, P, Hkv, 256]: box = one d-half (128 B) x 1 head x P rows
-// x 1 page, 128-byte swizzle.
-bool make_cache_tmap(CUtensorMap* m, const pg_tensor* t, int P) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) {
-    set_tc_error("cuTensorMapEncodeTiled unavailable");
-    return false;
-  }
-  cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1], (cuuint64_t)t->shape[0]};
-  cuuint64_t strides[3] = {(cuuint64_t)t->stride[2], (cuuint64_t)t->stride[1], (cuuint64_t)t->stride[0]};
-  cuuint32_t box[4] = {128, 1, (cuuint32_t)P, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, t->data, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    snprintf(t_tc_err, sizeof t_tc_err, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return false;
-  }
-  return true;
-}
-
-const char* tc_last_error() { return t_tc_err; }
-
 int launch_verify_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp, const pg_tensor* k,
                      const pg_tensor* v, int sms, cudaStream_t stream) {
   (void)sms;
@@ -728,15 +715,19 @@ int launch_verify_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp,
   if (dev >= 0 && dev < 64 && !(attr_done[dev] & which)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) {
-      snprintf(t_tc_err, sizeof t_tc_err, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+      char buf[160];
+      snprintf(buf, sizeof buf, "cudaFuncSetAttribute(verify): %s", cudaGetErrorString(e));
+      set_tc_error(buf);
       return -1;
     }
     attr_done[dev] |= which;
   }
-  kern<<<cp.num_ctas, kVThreads, kSmemBytes, stream>>>(tk, tv, p, ptr, cp);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, cp.num_ctas, kVThreads, kSmemBytes, stream, tk, tv, p, ptr, cp);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
-    snprintf(t_tc_err, sizeof t_tc_err, "verify kernel launch: %s", cudaGetErrorString(e));
+    char buf[160];
+    snprintf(buf, sizeof buf, "verify kernel launch: %s", cudaGetErrorString(e));
+    set_tc_error(buf);
     return -1;
   }
   return 1;
