@@ -57,26 +57,25 @@ constexpr uint32_t kQHalf = kRows * 128;        // [128 rows][128 B]
 constexpr uint32_t kQPart = 2 * kQHalf;         // 32 KB
 constexpr uint32_t kKVHalf = kTileKeys * 128;   // [128 keys][128 B]
 constexpr uint32_t kKVTile = 2 * kKVHalf;       // 32 KB
-constexpr uint32_t kPPart = kRows * kTileKeys;  // [128 rows][128 keys] e4m3 = 16 KB
-
-// TMEM columns: S double buffer (2 x 128), O d-half 0 and 1 (2 x 128).
+// TMEM columns: S double buffer (2 x 128), O d-half 0 and 1 (2 x 128). P of a tile replaces
+// the first 64 columns of its S buffer (P_hi 32, P_lo 32: four e4m3 keys per column) and
+// is the A operand of O += P V straight from TMEM.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
+constexpr uint32_t kPCols = kTileKeys / 4;  // 32 columns per P part
 
 constexpr uint32_t kIdescS = idesc_e4m3(128, 128, false, false);  // Q (K-major) x K (K-major)
-constexpr uint32_t kIdescO = idesc_e4m3(128, 128, false, true);   // P (K-major) x V (MN-major)
+constexpr uint32_t kIdescO = idesc_e4m3(128, 128, false, true);   // P (TMEM) x V (MN-major)
 
 template <bool kQFp8>
 struct Layout {
   static constexpr int kQParts = kQFp8 ? 1 : 2;
-  static constexpr int kVStages = kQFp8 ? 2 : 1;
+  static constexpr int kVStages = kQFp8 ? 3 : 2;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffK = kOffQ + kQParts * kQPart;
   static constexpr uint32_t kOffV = kOffK + kKStages * kKVTile;
-  static constexpr uint32_t kOffPhi = kOffV + kVStages * kKVTile;
-  static constexpr uint32_t kOffPlo = kOffPhi + kPPart;
-  static constexpr uint32_t kOffMisc = kOffPlo + kPPart;
+  static constexpr uint32_t kOffMisc = kOffV + kVStages * kKVTile;
 };
 
 struct Misc {
@@ -84,7 +83,8 @@ struct Misc {
   alignas(16) float lsum[2][kRows];     // [key half][row] row-sum halves (epilogue)
   alignas(16) long long out_off[2][kRows];
   alignas(16) int lim[2][kRows];
-  alignas(8) uint64_t k_full[kKStages], k_empty[kKStages], v_full[2], v_empty[2];
+  alignas(16) float merge_w[kMergeMaxSplits * kSlotRows];
+  alignas(8) uint64_t k_full[kKStages], k_empty[kKStages], v_full[3], v_empty[3];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full, p_free, q_full, q_free, o_ready, o_free, drain;
   float qscale[2];
@@ -206,7 +206,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     const uint64_t policy = policy_evict_first();
     const int ppt = kTileKeys / p.P;
     uint32_t g = 0;
-    uint32_t issued[2] = {0, 0};
+    uint32_t issued[kVStages > kKStages ? kVStages : kKStages] = {};
     bool stop = false;
     for (int it = item_begin; it < item_end && !stop; ++it) {
       const Item I = load_item(cp, ptr, it);
@@ -279,13 +279,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         const uint32_t st = t.g % kVStages;
         if (!mbar_wait(bar(ms.v_full[st]), (t.g / kVStages) & 1, abort_flag, ptr.err)) return false;
         tc_fence_after();
+        const uint32_t p_cols = tmem + kColS + (t.g & 1) * 128;  // P of this tile, in its S buffer
         for (int h = 0; h < 2; ++h) {
           for (int part = 0; part < 2; ++part) {
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = smem_desc(sbase + (part ? LY::kOffPlo : LY::kOffPhi) + kk * 32, 16, 1024, kSw128);
               const uint64_t b =
                   smem_desc(sbase + LY::kOffV + st * kKVTile + h * kKVHalf + kk * 4096, 1024, 1024, kSw128);
-              mma_e4m3(tmem + kColO + h * 128, a, b, kIdescO, (t.first && part == 0 && kk == 0) ? 0u : 1u);
+              mma_e4m3_ts(tmem + kColO + h * 128, p_cols + part * kPCols + kk * 8, b, kIdescO,
+                          (t.first && part == 0 && kk == 0) ? 0u : 1u);
             }
           }
         }
@@ -504,11 +505,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         }
         const float2 ls = __half22float2(__hadd2(__hadd2(acc[0], acc[1]), __hadd2(acc[2], acc[3])));
         l += ls.x + ls.y;
-        if (g >= 1 && !mbar_wait(bar(ms.p_free), (g - 1) & 1, abort_flag, ptr.err)) bad = true;
-        tc_fence_after();
         // tcgen05.ld/st are warp-collective: a warp rescales if any of its rows must,
-        // lanes whose row keeps its reference multiply by 1
-        if (__any_sync(0xffffffffu, rescale && j > 0)) {
+        // lanes whose row keeps its reference multiply by 1. O may only be touched once the
+        // previous tile's P.V has completed; otherwise that wait comes after publishing P
+        // (each tile waits exactly once, so the barrier's parity stays unambiguous).
+        const bool warp_rescale = __any_sync(0xffffffffu, rescale && j > 0);
+        if (warp_rescale) {
+          if (g >= 1 && !mbar_wait(bar(ms.p_free), (g - 1) & 1, abort_flag, ptr.err)) bad = true;
+          tc_fence_after();
           if (!(rescale && j > 0)) alpha = 1.f;
           // this thread's half of its O row: d-half kh
 #pragma unroll 1
@@ -535,19 +539,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             for (int i = 0; i < 8; ++i) dst[i] = z;
           }
         }
-        // P rows, K-major 128-byte swizzle: row `row`, 16-byte chunks 4*kh .. 4*kh+3
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const int chunk = kh * 4 + cc;
-          const uint32_t off2 = row * 128 + ((chunk ^ (row & 7)) << 4);
-          *reinterpret_cast<uint4*>(smem + LY::kOffPhi + off2) =
-              make_uint4(ph[4 * cc], ph[4 * cc + 1], ph[4 * cc + 2], ph[4 * cc + 3]);
-          *reinterpret_cast<uint4*>(smem + LY::kOffPlo + off2) =
-              make_uint4(pl[4 * cc], pl[4 * cc + 1], pl[4 * cc + 2], pl[4 * cc + 3]);
-        }
-        fence_proxy_async_smem();
+        // P into TMEM over this tile's S: row `row`, keys 64*kh .. 64*kh+63 -> columns
+        // 16*kh .. 16*kh+15 of P_hi (S columns 0..31) and P_lo (S columns 32..63)
+        tmem_st16u(tmem + lane_addr + kColS + b * 128 + kh * 16, ph);
+        tmem_st16u(tmem + lane_addr + kColS + b * 128 + kPCols + kh * 16, pl);
+        tmem_wait_st();
+        fence_proxy_async_smem();  // zeroed V rows, if any
         tc_fence_before();
         mbar_arrive(bar(ms.p_full));
+        if (!warp_rescale && g >= 1 && !mbar_wait(bar(ms.p_free), (g - 1) & 1, abort_flag, ptr.err)) bad = true;
       }
       if (it + 1 < item_end) q_prep(load_item(cp, ptr, it + 1), ii + 1);
 
@@ -596,9 +596,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         rb.nrows = I.nrows;
         rb.nsplit = I.nsplit;
         rb.slot_base = I.slot_base;
-        // the P buffers are idle until the next item's first tile: merge weights live there
-        finish_split_block(p, ptr, cp, I.block, rb, gi, kSoftThreads, 10, &ms.merge_flag,
-                           reinterpret_cast<float*>(smem + LY::kOffPhi));
+        finish_split_block(p, ptr, cp, I.block, rb, gi, kSoftThreads, 10, &ms.merge_flag, ms.merge_w);
       }
     }
   }
