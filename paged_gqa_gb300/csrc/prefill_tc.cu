@@ -203,7 +203,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     uint64_t* full = is_k ? ms.k_full : ms.v_full;
     uint64_t* empty = is_k ? ms.k_empty : ms.v_empty;
     if (lane == 0) tma_prefetch_desc(tmap);
-    const uint64_t policy = policy_evict_first();
+    // Every row block of a sequence re-reads the same K/V pages: keep them in L2.
+    const uint64_t policy = policy_evict_last();
     const int ppt = kTileKeys / p.P;
     uint32_t g = 0;
     uint32_t issued[kVStages > kKStages ? kVStages : kKStages] = {};
