@@ -13,14 +13,17 @@
 //     is one tcgen05.mma kind::f8f6f4 M=128 x N=128 keys x K=256 per tile (8 MMAs of
 //     K=32; bf16 Q is split once per block into e4m3 hi + lo and costs 16);
 //   * P = 2^(s - m + 4) is split into e4m3 hi + lo (about bf16 precision; a single e4m3 P
-//     misses the 5e-3 relative-L2 bar) and O += P V runs as M=128 x N=128 per d-half with
-//     V as an MN-major operand, fp32 accumulators in TMEM (O: 256 columns, S: 2 x 128);
+//     misses the 5e-3 relative-L2 bar), written into TMEM over the tile's S and used from
+//     there as the A operand of O += P V: M=128 x N=256 (all of d, V as an MN-major operand
+//     whose two 128-byte d-halves sit 16 KB apart), fp32 accumulators in TMEM (O: 256
+//     columns, S: 2 x 128);
 //   * online softmax with one row per TMEM lane: two threads share a row (64 keys each)
 //     and exchange their partial maxima; a row's reference only moves, and its O row is only
 //     rescaled, when a score exceeds the reference by 2^4;
 //   * K and V pages arrive by TMA (one box per page and d-half) from two producer warps;
-//     one thread issues the MMAs; persistent CTAs walk contiguous ranges of key tiles cut by
-//     the plan kernel, and blocks cut across CTAs are merged by their last piece.
+//     two threads issue the MMAs (S and P.V), since one thread issues tcgen05.mma slower
+//     than the tensor pipe retires them; persistent CTAs walk contiguous ranges of key
+//     tiles cut by the plan kernel, and blocks cut across CTAs are merged by their last piece.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -45,8 +48,9 @@ using namespace tc;
 constexpr int kRows = kPrefillRows;    // 128: MMA M
 constexpr int kSoftWarps = 8;
 constexpr int kSoftThreads = kSoftWarps * 32;
-constexpr int kThreads = 96 + kSoftThreads;    // + K producer, MMA, V producer warps
+constexpr int kThreads = 128 + kSoftThreads;   // + K producer, 2 MMA issuers, V producer
 constexpr int kVProducerWarp = 2 + kSoftWarps;
+constexpr int kPVIssuerWarp = 3 + kSoftWarps;
 constexpr int kHalfKeys = kTileKeys / 2;       // keys per softmax thread
 constexpr int kKStages = 2;
 constexpr float kTau = 4.f;
@@ -66,7 +70,7 @@ constexpr uint32_t kColO = 256;
 constexpr uint32_t kPCols = kTileKeys / 4;  // 32 columns per P part
 
 constexpr uint32_t kIdescS = idesc_e4m3(128, 128, false, false);  // Q (K-major) x K (K-major)
-constexpr uint32_t kIdescO = idesc_e4m3(128, 128, false, true);   // P (TMEM) x V (MN-major)
+constexpr uint32_t kIdescO = idesc_e4m3(128, 256, false, true);   // P (TMEM) x V (MN-major, N = d = 256)
 
 template <bool kQFp8>
 struct Layout {
@@ -85,8 +89,8 @@ struct Misc {
   alignas(16) int lim[2][kRows];
   alignas(16) float merge_w[kMergeMaxSplits * kSlotRows];
   alignas(8) uint64_t k_full[kKStages], k_empty[kKStages], v_full[3], v_empty[3];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, p_free, q_full, q_free, o_ready, o_free, drain;
+  uint64_t s_full[2], pv_done[2];
+  uint64_t p_full, q_full, q_free, o_ready, o_free, drain[2];
   float qscale[2];
   float amax[kSoftWarps];
   uint32_t tmem_base;
@@ -167,15 +171,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(ms.s_full[b]), 1);
-      mbar_init(bar(ms.s_free[b]), kSoftThreads);
+      mbar_init(bar(ms.pv_done[b]), 1);
     }
     mbar_init(bar(ms.p_full), kSoftThreads);
-    mbar_init(bar(ms.p_free), 1);
     mbar_init(bar(ms.q_full), kSoftThreads);
     mbar_init(bar(ms.q_free), 1);
     mbar_init(bar(ms.o_ready), 1);
     mbar_init(bar(ms.o_free), kSoftThreads);
-    mbar_init(bar(ms.drain), 1);
+    mbar_init(bar(ms.drain[0]), 1);
+    mbar_init(bar(ms.drain[1]), 1);
     ms.abort_flag = 0;
     fence_mbar_init();
   }
@@ -264,64 +268,66 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         if (issued[s]) mbar_wait(bar(full[s]), (issued[s] - 1) & 1, abort_flag, ptr.err);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kPVIssuerWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread cannot issue tcgen05.mma faster than about one per 44 ns, below the tensor
+    // pipe's rate, so S = Q K^T and O += P V come from two warps. P of tile g lives in S
+    // buffer g & 1, so S(g) waits for P.V(g-2); P.V(g) waits for P(g) and V(g).
     if (lane == 0) {
+      const bool is_s = warp == 1;
       uint32_t g = 0;
       int ii = 0;
-      struct Pending {
-        uint32_t g;
-        int first, last, item;
-      } pend = {0, 0, 0, -1};
       bool ok = true;
-      auto issue_pv = [&](const Pending& t) -> bool {
-        if (t.first && t.item >= 1 && !mbar_wait(bar(ms.o_free), (t.item - 1) & 1, abort_flag, ptr.err)) return false;
-        if (!mbar_wait(bar(ms.p_full), t.g & 1, abort_flag, ptr.err)) return false;
-        const uint32_t st = t.g % kVStages;
-        if (!mbar_wait(bar(ms.v_full[st]), (t.g / kVStages) & 1, abort_flag, ptr.err)) return false;
-        tc_fence_after();
-        const uint32_t p_cols = tmem + kColS + (t.g & 1) * 128;  // P of this tile, in its S buffer
-        for (int h = 0; h < 2; ++h) {
-          for (int part = 0; part < 2; ++part) {
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t b =
-                  smem_desc(sbase + LY::kOffV + st * kKVTile + h * kKVHalf + kk * 4096, 1024, 1024, kSw128);
-              mma_e4m3_ts(tmem + kColO + h * 128, p_cols + part * kPCols + kk * 8, b, kIdescO,
-                          (t.first && part == 0 && kk == 0) ? 0u : 1u);
-            }
-          }
-        }
-        mma_commit(bar(ms.v_empty[st]));
-        mma_commit(bar(ms.p_free));
-        if (t.last) mma_commit(bar(ms.o_ready));
-        return true;
-      };
       for (int it = item_begin; it < item_end && ok; ++it, ++ii) {
         const Item I = load_item(cp, ptr, it);
         for (int j = 0; j < I.ntiles && ok; ++j, ++g) {
-          if (j == 0 && !(ok = mbar_wait(bar(ms.q_full), ii & 1, abort_flag, ptr.err))) break;
-          const uint32_t st = g % kKStages, b = g & 1;
-          if (!(ok = mbar_wait(bar(ms.k_full[st]), (g / kKStages) & 1, abort_flag, ptr.err))) break;
-          if (g >= 2 && !(ok = mbar_wait(bar(ms.s_free[b]), ((g >> 1) - 1) & 1, abort_flag, ptr.err))) break;
-          tc_fence_after();
-          for (int part = 0; part < LY::kQParts; ++part) {
-            for (int kb = 0; kb < 8; ++kb) {
-              const int h = kb >> 2, kk = kb & 3;
-              const uint64_t a = smem_desc(sbase + LY::kOffQ + part * kQPart + h * kQHalf + kk * 32, 16, 1024, kSw128);
-              const uint64_t bk = smem_desc(sbase + LY::kOffK + st * kKVTile + h * kKVHalf + kk * 32, 16, 1024, kSw128);
-              mma_e4m3(tmem + kColS + b * 128, a, bk, kIdescS, (part | kb) ? 1u : 0u);
+          const uint32_t b = g & 1;
+          if (is_s) {
+            if (j == 0 && !(ok = mbar_wait(bar(ms.q_full), ii & 1, abort_flag, ptr.err))) break;
+            const uint32_t st = g % kKStages;
+            if (!(ok = mbar_wait(bar(ms.k_full[st]), (g / kKStages) & 1, abort_flag, ptr.err))) break;
+            if (g >= 2 && !(ok = mbar_wait(bar(ms.pv_done[b]), ((g >> 1) - 1) & 1, abort_flag, ptr.err))) break;
+            tc_fence_after();
+            const uint64_t k0 = smem_desc(sbase + LY::kOffK + st * kKVTile, 16, 1024, kSw128);
+#pragma unroll
+            for (int part = 0; part < LY::kQParts; ++part) {
+              const uint64_t q0 = smem_desc(sbase + LY::kOffQ + part * kQPart, 16, 1024, kSw128);
+#pragma unroll
+              for (int kb = 0; kb < 8; ++kb) {
+                const uint32_t qoff = (kb >> 2) * kQHalf + (kb & 3) * 32, koff = (kb >> 2) * kKVHalf + (kb & 3) * 32;
+                mma_e4m3(tmem + kColS + b * 128, q0 + (qoff >> 4), k0 + (koff >> 4), kIdescS, (part | kb) ? 1u : 0u);
+              }
             }
+            mma_commit(bar(ms.s_full[b]));
+            mma_commit(bar(ms.k_empty[st]));
+            if (j == I.ntiles - 1) mma_commit(bar(ms.q_free));
+          } else {
+            // the first P.V of an item overwrites O: the previous epilogue must be done
+            if (j == 0 && ii >= 1 && !(ok = mbar_wait(bar(ms.o_free), (ii - 1) & 1, abort_flag, ptr.err))) break;
+            if (!(ok = mbar_wait(bar(ms.p_full), g & 1, abort_flag, ptr.err))) break;
+            const uint32_t st = g % kVStages;
+            if (!(ok = mbar_wait(bar(ms.v_full[st]), (g / kVStages) & 1, abort_flag, ptr.err))) break;
+            tc_fence_after();
+            // V as one N = 256 MN-major operand: d-half 1 is the second 128-byte atom, 16 KB on
+            const uint64_t v0 = smem_desc(sbase + LY::kOffV + st * kKVTile, kKVHalf, 1024, kSw128);
+            const uint32_t p_cols = tmem + kColS + b * 128;  // P of this tile, in its S buffer
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_e4m3_ts(tmem + kColO, p_cols + part * kPCols + kk * 8, v0 + ((kk * 4096) >> 4), kIdescO,
+                            (j == 0 && part == 0 && kk == 0) ? 0u : 1u);
+            }
+            mma_commit(bar(ms.v_empty[st]));
+            mma_commit(bar(ms.pv_done[b]));
+            if (j == I.ntiles - 1) mma_commit(bar(ms.o_ready));
           }
-          mma_commit(bar(ms.s_full[b]));
-          mma_commit(bar(ms.k_empty[st]));
-          if (j == I.ntiles - 1) mma_commit(bar(ms.q_free));
-          if (pend.item >= 0 && !(ok = issue_pv(pend))) break;
-          pend = {g, j == 0, j == I.ntiles - 1, ii};
         }
       }
-      if (ok && pend.item >= 0) issue_pv(pend);
-      mma_commit(bar(ms.drain));
-      mbar_wait(bar(ms.drain), 0, abort_flag, ptr.err);
+      // Every MMA this thread issued has completed before the CTA may release TMEM.
+      uint64_t& drain = is_s ? ms.drain[0] : ms.drain[1];
+      mma_commit(bar(drain));
+      mbar_wait(bar(drain), 0, abort_flag, ptr.err);
     }
     __syncwarp();
   } else if (warp >= 2 && warp < kVProducerWarp) {
@@ -459,8 +465,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           for (int i = 0; i < 16; ++i) t[k + i] = v[i];
         }
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(ms.s_free[b]));
         // masked tiles hold scaled scores; unmasked tiles keep raw scores and take the
         // scale in the exponent's FFMA
         const bool need_mask = (key0 + kTileKeys > kv_hi) || (key0 + kTileKeys - 1 > min_lim);
@@ -512,7 +516,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         // (each tile waits exactly once, so the barrier's parity stays unambiguous).
         const bool warp_rescale = __any_sync(0xffffffffu, rescale && j > 0);
         if (warp_rescale) {
-          if (g >= 1 && !mbar_wait(bar(ms.p_free), (g - 1) & 1, abort_flag, ptr.err)) bad = true;
+          if (g >= 1 && !mbar_wait(bar(ms.pv_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, abort_flag, ptr.err)) bad = true;
           tc_fence_after();
           if (!(rescale && j > 0)) alpha = 1.f;
           // this thread's half of its O row: d-half kh
@@ -548,7 +552,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         fence_proxy_async_smem();  // zeroed V rows, if any
         tc_fence_before();
         mbar_arrive(bar(ms.p_full));
-        if (!warp_rescale && g >= 1 && !mbar_wait(bar(ms.p_free), (g - 1) & 1, abort_flag, ptr.err)) bad = true;
+        // P.V(g-1) has a barrier of its own (its S buffer's), whose next phase needs P(g+1):
+        // the wait cannot mistake a later phase for this one, however late it runs.
+        if (!warp_rescale && g >= 1 &&
+            !mbar_wait(bar(ms.pv_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, abort_flag, ptr.err))
+          bad = true;
       }
       if (it + 1 < item_end) q_prep(load_item(cp, ptr, it + 1), ii + 1);
 

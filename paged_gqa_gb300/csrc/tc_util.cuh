@@ -6,6 +6,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include "common.cuh"
 
 namespace pgqa {

@@ -23,11 +23,14 @@
 //     reduction (redux.sync + shared memory). It is only taken when some score exceeds the
 //     running reference by 2^4 (the reference then moves to the exact max and O^T and the
 //     row sums are rescaled); otherwise P = 2^(s - m + 4) <= 256 fits e4m3 directly;
+//   * S and P.V are issued by two threads: one thread issues tcgen05.mma at about one per
+//     44 ns, slower than the tensor pipe retires these shapes, and S can then run ahead of
+//     the softmax while P.V of the previous tile completes;
 //   * persistent CTAs (one per SM) walk a contiguous range of key tiles cut by the plan
 //     kernel; a block cut across CTAs is finished by the last piece with a log-sum-exp merge.
 //
-// Warp roles (352 threads): warp 0 = K producer (TMA), warp 1 = MMA issuer (+ TMEM owner),
-// warps 2-9 = softmax and epilogue, warp 10 = V producer (TMA). Softmax thread (q, c, lane)
+// Warp roles (384 threads): warp 0 = K producer (TMA), warp 1 = S issuer (+ TMEM owner),
+// warps 2-9 = softmax and epilogue, warp 10 = V producer (TMA), warp 11 = P.V issuer. Softmax thread (q, c, lane)
 // owns TMEM lane 32q+lane (= key of the tile, = d within a d-half for O^T) and rows
 // [32c, 32c+32). Shared memory: Q hi/lo 32 KB, 2 K stages and 3 V stages of 32 KB, P hi/lo
 // 16 KB, barriers and row state (~221 KB, one CTA per SM). TMEM: 2 S buffers of 128
@@ -53,8 +56,9 @@ using namespace tc;
 constexpr int kVN = 64;            // query rows of a verify block (MMA N per Q or P part)
 constexpr int kSoftWarps = 8;
 constexpr int kSoftThreads = kSoftWarps * 32;
-constexpr int kVThreads = 96 + kSoftThreads;  // + K producer, MMA, V producer warps
+constexpr int kVThreads = 128 + kSoftThreads;  // + K producer, 2 MMA issuers, V producer
 constexpr int kVProducerWarp = 2 + kSoftWarps;
+constexpr int kPVIssuerWarp = 3 + kSoftWarps;
 constexpr int kCols = kVN / 2;     // rows per softmax thread
 constexpr int kKStages = 2;        // K tiles in shared memory (freed by S = K Q^T)
 constexpr int kVStages = 3;        // V tiles in shared memory (held until O += P V)
@@ -95,7 +99,7 @@ struct Misc {
   alignas(16) float merge_w[kMergeMaxSplits * kSlotRows];
   alignas(8) uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], s_free[2];
-  uint64_t p_full, p_free, q_full, q_free, o_ready, o_free, drain;
+  uint64_t p_full, p_free, q_full, q_free, o_ready, o_free, drain[2];
   float qscale[2];
   float amax[kSoftWarps];
   uint32_t tmem_base;
@@ -184,7 +188,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     mbar_init(bar(ms.q_free), 1);
     mbar_init(bar(ms.o_ready), 1);
     mbar_init(bar(ms.o_free), kSoftThreads);
-    mbar_init(bar(ms.drain), 1);
+    mbar_init(bar(ms.drain[0]), 1);
+    mbar_init(bar(ms.drain[1]), 1);
     ms.abort_flag = 0;
     fence_mbar_init();
   }
@@ -276,59 +281,64 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         if (issued[s]) mbar_wait(bar(full[s]), (issued[s] - 1) & 1, abort_flag, ptr.err);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kPVIssuerWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread cannot issue tcgen05.mma faster than about one per 44 ns, below the tensor
+    // pipe's rate for these shapes, so S = K Q^T and O^T += V^T P^T come from two warps:
+    // S runs ahead as soon as a K tile and an S buffer are free, P.V as soon as P is
+    // published. The two streams share no operand or accumulator.
     if (lane == 0) {
+      const bool is_s = warp == 1;
       uint32_t g = 0;
       int ii = 0;
-      struct Pending {
-        uint32_t g;
-        int first, last, item;
-      } pend = {0, 0, 0, -1};
       bool ok = true;
-      auto issue_pv = [&](const Pending& t) -> bool {
-        if (t.first && t.item >= 1 && !mbar_wait(bar(ms.o_free), (t.item - 1) & 1, abort_flag, ptr.err)) return false;
-        if (!mbar_wait(bar(ms.p_full), t.g & 1, abort_flag, ptr.err)) return false;
-        const uint32_t st = t.g % kVStages;
-        if (!mbar_wait(bar(ms.v_full[st]), (t.g / kVStages) & 1, abort_flag, ptr.err)) return false;
-        tc_fence_after();
-        for (int h = 0; h < 2; ++h) {
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = smem_desc(sbase + kOffV + st * kKVTile + h * kKVHalf + kk * 4096, 1024, 1024, kSw128);
-            const uint64_t b = smem_desc(sbase + kOffP + kk * 4096, 1024, 1024, kSw128);
-            mma_e4m3(tmem + kColO + h * 128, a, b, kIdescO, (t.first && kk == 0) ? 0u : 1u);
-          }
-        }
-        mma_commit(bar(ms.v_empty[st]));
-        mma_commit(bar(ms.p_free));
-        if (t.last) mma_commit(bar(ms.o_ready));
-        return true;
-      };
       for (int it = item_begin; it < item_end && ok; ++it, ++ii) {
         const Item I = load_item(cp, ptr, it);
         for (int j = 0; j < I.ntiles && ok; ++j, ++g) {
-          if (j == 0 && !(ok = mbar_wait(bar(ms.q_full), ii & 1, abort_flag, ptr.err))) break;
-          const uint32_t st = g % kKStages, b = g & 1;
-          if (!(ok = mbar_wait(bar(ms.k_full[st]), (g / kKStages) & 1, abort_flag, ptr.err))) break;
-          if (g >= 2 && !(ok = mbar_wait(bar(ms.s_free[b]), ((g >> 1) - 1) & 1, abort_flag, ptr.err))) break;
-          tc_fence_after();
-          for (int kb = 0; kb < 8; ++kb) {
-            const int h = kb >> 2, kk = kb & 3;
-            const uint64_t a = smem_desc(sbase + kOffK + st * kKVTile + h * kKVHalf + kk * 32, 16, 1024, kSw128);
-            const uint64_t bq = smem_desc(sbase + kOffQ + h * kQHalf + kk * 32, 16, 1024, kSw128);
-            mma_e4m3(tmem + kColS + b * 128, a, bq, kIdescS, kb ? 1u : 0u);
+          if (is_s) {
+            if (j == 0 && !(ok = mbar_wait(bar(ms.q_full), ii & 1, abort_flag, ptr.err))) break;
+            const uint32_t st = g % kKStages, b = g & 1;
+            if (!(ok = mbar_wait(bar(ms.k_full[st]), (g / kKStages) & 1, abort_flag, ptr.err))) break;
+            if (g >= 2 && !(ok = mbar_wait(bar(ms.s_free[b]), ((g >> 1) - 1) & 1, abort_flag, ptr.err))) break;
+            tc_fence_after();
+            const uint64_t a0 = smem_desc(sbase + kOffK + st * kKVTile, 16, 1024, kSw128);
+            const uint64_t b0 = smem_desc(sbase + kOffQ, 16, 1024, kSw128);
+#pragma unroll
+            for (int kb = 0; kb < 8; ++kb) {
+              const uint32_t off = (kb >> 2) * kKVHalf + (kb & 3) * 32, qoff = (kb >> 2) * kQHalf + (kb & 3) * 32;
+              mma_e4m3(tmem + kColS + b * 128, a0 + (off >> 4), b0 + (qoff >> 4), kIdescS, kb ? 1u : 0u);
+            }
+            mma_commit(bar(ms.s_full[b]));
+            mma_commit(bar(ms.k_empty[st]));
+            if (j == I.ntiles - 1) mma_commit(bar(ms.q_free));
+          } else {
+            // the first P.V of an item overwrites O^T: the previous epilogue must be done
+            if (j == 0 && ii >= 1 && !(ok = mbar_wait(bar(ms.o_free), (ii - 1) & 1, abort_flag, ptr.err))) break;
+            if (!(ok = mbar_wait(bar(ms.p_full), g & 1, abort_flag, ptr.err))) break;
+            const uint32_t st = g % kVStages;
+            if (!(ok = mbar_wait(bar(ms.v_full[st]), (g / kVStages) & 1, abort_flag, ptr.err))) break;
+            tc_fence_after();
+            const uint64_t a0 = smem_desc(sbase + kOffV + st * kKVTile, 1024, 1024, kSw128);
+            const uint64_t b0 = smem_desc(sbase + kOffP, 1024, 1024, kSw128);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t off = h * kKVHalf + kk * 4096, poff = kk * 4096;
+                mma_e4m3(tmem + kColO + h * 128, a0 + (off >> 4), b0 + (poff >> 4), kIdescO,
+                         (j == 0 && kk == 0) ? 0u : 1u);
+              }
+            }
+            mma_commit(bar(ms.v_empty[st]));
+            mma_commit(bar(ms.p_free));
+            if (j == I.ntiles - 1) mma_commit(bar(ms.o_ready));
           }
-          mma_commit(bar(ms.s_full[b]));
-          mma_commit(bar(ms.k_empty[st]));
-          if (j == I.ntiles - 1) mma_commit(bar(ms.q_free));
-          if (pend.item >= 0 && !(ok = issue_pv(pend))) break;
-          pend = {g, j == 0, j == I.ntiles - 1, ii};
         }
       }
-      if (ok && pend.item >= 0) issue_pv(pend);
-      // Wait for every MMA issued by this thread before the CTA may release TMEM.
-      mma_commit(bar(ms.drain));
-      mbar_wait(bar(ms.drain), 0, abort_flag, ptr.err);
+      // Every MMA this thread issued has completed before the CTA may release TMEM.
+      uint64_t& drain = is_s ? ms.drain[0] : ms.drain[1];
+      mma_commit(bar(drain));
+      mbar_wait(bar(drain), 0, abort_flag, ptr.err);
     }
     __syncwarp();
   } else if (warp >= 2 && warp < kVProducerWarp) {
@@ -475,8 +485,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         tc_fence_after();
         load_s(b, t);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(ms.s_free[b]));
         // x = s c - m + sigma: the exponent of P, one FFMA per score
         const bool need_mask = (key0 + kTileKeys > I.kv_hi) || (key0 + kTileKeys - 1 > min_lim);
         float xmax = -INFINITY;
@@ -517,9 +525,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
         const bool rescale = votes & 1;
         if (rescale) {
-          // Reload the raw scores (S buffer b is only overwritten after this tile's P is
-          // published; x may have lost s entirely against a -1e30 reference), take the
-          // exact tile maximum of s c per row, then the new reference.
+          // Reload the raw scores (S buffer b is released only after this block; x may have
+          // lost s entirely against a -1e30 reference), take the exact tile maximum of s c
+          // per row, then the new reference.
           tc_fence_after();
           load_s(b, t);
           tmem_wait_ld();
@@ -548,6 +556,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             l[n] *= ms.alpha[c0 + n];
           }
         }
+        // S buffer b is read for the last time above (the rescale path reloads it): only now
+        // may the S issuer overwrite it with S(g+2)
+        tc_fence_before();
+        mbar_arrive(bar(ms.s_free[b]));
         // P = 2^x in f16, split into e4m3 hi + lo (4 rows per word); row sums in fp32
         uint32_t ph[kCols / 4], pl[kCols / 4];
 #pragma unroll
