@@ -29,8 +29,9 @@
 //   * persistent CTAs (one per SM) walk a contiguous range of key tiles cut by the plan
 //     kernel; a block cut across CTAs is finished by the last piece with a log-sum-exp merge.
 //
-// Warp roles (384 threads): warp 0 = K producer (TMA), warp 1 = S issuer (+ TMEM owner),
-// warps 2-9 = softmax and epilogue, warp 10 = V producer (TMA), warp 11 = P.V issuer. Softmax thread (q, c, lane)
+// Warp roles (512 threads): warp 0 = S issuer (+ TMEM owner), warp 1 = P.V issuer, warps
+// 2, 3, 12 = K producers (TMA), warps 4-11 = softmax and epilogue, warps 13-15 = V
+// producers (TMA). Softmax thread (q, c, lane)
 // owns TMEM lane 32q+lane (= key of the tile, = d within a d-half for O^T) and rows
 // [32c, 32c+32). Shared memory: Q hi/lo 32 KB, 2 K stages and 3 V stages of 32 KB, P hi/lo
 // 16 KB, barriers and row state (~221 KB, one CTA per SM). TMEM: 2 S buffers of 128
@@ -56,9 +57,16 @@ using namespace tc;
 constexpr int kVN = 64;            // query rows of a verify block (MMA N per Q or P part)
 constexpr int kSoftWarps = 8;
 constexpr int kSoftThreads = kSoftWarps * 32;
-constexpr int kVThreads = 128 + kSoftThreads;  // + K producer, 2 MMA issuers, V producer
-constexpr int kVProducerWarp = 2 + kSoftWarps;
-constexpr int kPVIssuerWarp = 3 + kSoftWarps;
+// 16 warps in four warpgroups. Warpgroup 0: warp 0 = S issuer (+ TMEM owner), warp 1 =
+// P.V issuer, warps 2-3 = K producers; warpgroups 1-2 (warps 4-11) = softmax; warpgroup 3:
+// warp 12 = K producer, warps 13-15 = V producers. The softmax warpgroups take 192
+// registers per thread, the others 64 (setmaxnreg): 2 x 128 x 192 + 2 x 128 x 64 = 65536.
+constexpr int kVThreads = 512;
+constexpr int kLaunchRegs = 65536 / kVThreads;  // 128: what the split above redistributes
+constexpr int kSoftRegs = 192, kOtherRegs = 64;
+static_assert(2 * 128 * kSoftRegs + 2 * 128 * kOtherRegs == kVThreads * kLaunchRegs, "register split");
+constexpr int kSoftWarp0 = 4;
+constexpr int kProdPerOp = 3;  // TMA producer warps per operand (one thread issues too slowly)
 constexpr int kCols = kVN / 2;     // rows per softmax thread
 constexpr int kKStages = 2;        // K tiles in shared memory (freed by S = K Q^T)
 constexpr int kVStages = 3;        // V tiles in shared memory (held until O += P V)
@@ -171,11 +179,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKStages; ++s) {
-      mbar_init(bar(ms.k_full[s]), 1);
+      mbar_init(bar(ms.k_full[s]), kProdPerOp);
       mbar_init(bar(ms.k_empty[s]), 1);
     }
     for (int s = 0; s < kVStages; ++s) {
-      mbar_init(bar(ms.v_full[s]), 1);
+      mbar_init(bar(ms.v_full[s]), kProdPerOp);
       mbar_init(bar(ms.v_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -193,7 +201,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     ms.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 0) {
     tmem_alloc(smem_u32(&ms.tmem_base), kTmemCols);
     tmem_relinquish();
   }
@@ -208,142 +216,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   const int item_end = cp.cta_item_begin[blockIdx.x + 1];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  if (warp == 0 || warp == kVProducerWarp) {
-    // ------------------------------------------------------------ TMA producers (K, V)
-    // Two independent warps, so K tiles run ahead as soon as S = K Q^T frees a stage,
-    // whatever the P.V of older tiles is doing.
-    const bool is_k = warp == 0;
-    const CUtensorMap* tmap = is_k ? &tmap_k : &tmap_v;
-    const int nst = is_k ? kKStages : kVStages;
-    const uint32_t region = sbase + (is_k ? kOffK : kOffV);
-    uint64_t* full = is_k ? ms.k_full : ms.v_full;
-    uint64_t* empty = is_k ? ms.k_empty : ms.v_empty;
-    if (lane == 0) tma_prefetch_desc(tmap);
-    const uint64_t policy = policy_evict_first();
-    const int ppt = kTileKeys / p.P;  // pages per tile (1, 2, 4 or 8); 32 is a multiple
-    uint32_t g = 0;
-    uint32_t issued[kVStages] = {};
-    bool stop = false;
-    for (int it = item_begin; it < item_end && !stop; ++it) {
-      const Item I = load_item(cp, ptr, it);
-      const int32_t* bt_row = ptr.block_table + (size_t)I.seq * p.bt_stride;
-      const int page0 = I.tile_begin * ppt;                 // first page of the piece
-      const int npages = (I.kv_hi + p.P - 1) / p.P - page0; // pages the piece reads
-      // a window of 32 block-table entries, one per lane, and the next one in flight
-      auto fetch = [&](int w) -> int {
-        const int pg = w * 32 + lane;
-        int blk = -1;
-        if (pg < npages) {
-          blk = bt_row[page0 + pg];
-          if (blk < 0 || blk >= p.NB) {
-            atomicOr(ptr.err, kErrPage);
-            blk = 0;
-          }
-        }
-        return blk;
-      };
-      int cur = fetch(0), nxt = fetch(1);
-      int cur_w = 0;
-      for (int j = 0; j < I.ntiles; ++j, ++g) {
-        const int first = j * ppt;  // page of this tile, relative to the piece
-        if (first / 32 != cur_w) {
-          cur = nxt;
-          cur_w = first / 32;
-          nxt = fetch(cur_w + 1);
-        }
-        const int tile_pages = min(ppt, npages - first);
-        const uint32_t st = g % nst, ph = (g / nst) & 1;
-        int ok = 1;
-        if (lane == 0) {
-          ok = mbar_wait(bar(empty[st]), ph ^ 1, abort_flag, ptr.err);
-          if (ok) mbar_expect_tx(bar(full[st]), (uint32_t)tile_pages * p.P * 128u * 2u);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          stop = true;
-          break;
-        }
-        for (int pg = 0; pg < tile_pages; ++pg) {
-          const int blk = __shfl_sync(0xffffffffu, cur, (first + pg) & 31);
-          if (lane == 0) {
-            const uint32_t row = (uint32_t)pg * p.P * 128u;
-            for (int h = 0; h < 2; ++h)
-              tma_load_4d(region + st * kKVTile + h * kKVHalf + row, tmap, h * 128, I.kvh, 0, blk, bar(full[st]),
-                          policy);
-          }
-        }
-        issued[st] = g / nst + 1;
-      }
-    }
-    // Every issued copy has landed before the CTA may exit.
-    if (lane == 0) {
-      for (int s = 0; s < nst; ++s)
-        if (issued[s]) mbar_wait(bar(full[s]), (issued[s] - 1) & 1, abort_flag, ptr.err);
-    }
-    __syncwarp();
-  } else if (warp == 1 || warp == kPVIssuerWarp) {
-    // ------------------------------------------------------------ MMA issuers
-    // One thread cannot issue tcgen05.mma faster than about one per 44 ns, below the tensor
-    // pipe's rate for these shapes, so S = K Q^T and O^T += V^T P^T come from two warps:
-    // S runs ahead as soon as a K tile and an S buffer are free, P.V as soon as P is
-    // published. The two streams share no operand or accumulator.
-    if (lane == 0) {
-      const bool is_s = warp == 1;
-      uint32_t g = 0;
-      int ii = 0;
-      bool ok = true;
-      for (int it = item_begin; it < item_end && ok; ++it, ++ii) {
-        const Item I = load_item(cp, ptr, it);
-        for (int j = 0; j < I.ntiles && ok; ++j, ++g) {
-          if (is_s) {
-            if (j == 0 && !(ok = mbar_wait(bar(ms.q_full), ii & 1, abort_flag, ptr.err))) break;
-            const uint32_t st = g % kKStages, b = g & 1;
-            if (!(ok = mbar_wait(bar(ms.k_full[st]), (g / kKStages) & 1, abort_flag, ptr.err))) break;
-            if (g >= 2 && !(ok = mbar_wait(bar(ms.s_free[b]), ((g >> 1) - 1) & 1, abort_flag, ptr.err))) break;
-            tc_fence_after();
-            const uint64_t a0 = smem_desc(sbase + kOffK + st * kKVTile, 16, 1024, kSw128);
-            const uint64_t b0 = smem_desc(sbase + kOffQ, 16, 1024, kSw128);
-#pragma unroll
-            for (int kb = 0; kb < 8; ++kb) {
-              const uint32_t off = (kb >> 2) * kKVHalf + (kb & 3) * 32, qoff = (kb >> 2) * kQHalf + (kb & 3) * 32;
-              mma_e4m3(tmem + kColS + b * 128, a0 + (off >> 4), b0 + (qoff >> 4), kIdescS, kb ? 1u : 0u);
-            }
-            mma_commit(bar(ms.s_full[b]));
-            mma_commit(bar(ms.k_empty[st]));
-            if (j == I.ntiles - 1) mma_commit(bar(ms.q_free));
-          } else {
-            // the first P.V of an item overwrites O^T: the previous epilogue must be done
-            if (j == 0 && ii >= 1 && !(ok = mbar_wait(bar(ms.o_free), (ii - 1) & 1, abort_flag, ptr.err))) break;
-            if (!(ok = mbar_wait(bar(ms.p_full), g & 1, abort_flag, ptr.err))) break;
-            const uint32_t st = g % kVStages;
-            if (!(ok = mbar_wait(bar(ms.v_full[st]), (g / kVStages) & 1, abort_flag, ptr.err))) break;
-            tc_fence_after();
-            const uint64_t a0 = smem_desc(sbase + kOffV + st * kKVTile, 1024, 1024, kSw128);
-            const uint64_t b0 = smem_desc(sbase + kOffP, 1024, 1024, kSw128);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t off = h * kKVHalf + kk * 4096, poff = kk * 4096;
-                mma_e4m3(tmem + kColO + h * 128, a0 + (off >> 4), b0 + (poff >> 4), kIdescO,
-                         (j == 0 && kk == 0) ? 0u : 1u);
-              }
-            }
-            mma_commit(bar(ms.v_empty[st]));
-            mma_commit(bar(ms.p_free));
-            if (j == I.ntiles - 1) mma_commit(bar(ms.o_ready));
-          }
-        }
-      }
-      // Every MMA this thread issued has completed before the CTA may release TMEM.
-      uint64_t& drain = is_s ? ms.drain[0] : ms.drain[1];
-      mma_commit(bar(drain));
-      mbar_wait(bar(drain), 0, abort_flag, ptr.err);
-    }
-    __syncwarp();
-  } else if (warp >= 2 && warp < kVProducerWarp) {
+  // Warpgroup roles. setmaxnreg is executed by all four warps of a warpgroup, first thing
+  // in its role's branch (the launcher checks that the kernel starts with kLaunchRegs).
+  const int wg = warp >> 2;
+  if (wg == 1 || wg == 2) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftRegs));
     // ------------------------------------------------------------ softmax + epilogue
-    const int sw = warp - 2;                 // 0..7
+    const int sw = warp - kSoftWarp0;        // 0..7
     const int gi = sw * 32 + lane;           // 0..255
     const int q4 = warp & 3;                 // TMEM lane quarter
     const int c0 = (sw >> 2) * kCols;        // first row (column) this thread owns
@@ -702,11 +581,154 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
       for (int n = 0; n < kCols; ++n) l[n] = 0.f;
     }
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+    const bool k_prod = warp == 2 || warp == 3 || warp == 12;
+    const bool v_prod = warp >= 13;
+    if (k_prod || v_prod) {
+      // ------------------------------------------------------------ TMA producers (K, V)
+      // K and V have their own warps, so K tiles run ahead as soon as S = K Q^T frees a
+      // stage, whatever the P.V of older tiles is doing; kProdPerOp warps share each tile
+      // (producer i takes the pages whose index in the tile is i mod kProdPerOp, both
+      // d-halves back to back), since one thread issues page-sized boxes too slowly to keep
+      // HBM busy.
+      const bool is_k = k_prod;
+      const int pi = is_k ? (warp == 12 ? 2 : warp - 2) : warp - 13;
+      const CUtensorMap* tmap = is_k ? &tmap_k : &tmap_v;
+      const int nst = is_k ? kKStages : kVStages;
+      const uint32_t region = sbase + (is_k ? kOffK : kOffV);
+      uint64_t* full = is_k ? ms.k_full : ms.v_full;
+      uint64_t* empty = is_k ? ms.k_empty : ms.v_empty;
+      if (lane == 0) tma_prefetch_desc(tmap);
+      const uint64_t policy = policy_evict_first();
+      const int ppt = kTileKeys / p.P;  // pages per tile (1, 2, 4 or 8); 32 is a multiple
+      uint32_t g = 0;
+      uint32_t issued[kVStages > kKStages ? kVStages : kKStages] = {};
+      bool stop = false;
+      for (int it = item_begin; it < item_end && !stop; ++it) {
+        const Item I = load_item(cp, ptr, it);
+        const int32_t* bt_row = ptr.block_table + (size_t)I.seq * p.bt_stride;
+        const int page0 = I.tile_begin * ppt;                 // first page of the piece
+        const int npages = (I.kv_hi + p.P - 1) / p.P - page0; // pages the piece reads
+        // a window of 32 block-table entries, one per lane, and the next one in flight
+        auto fetch = [&](int w) -> int {
+          const int pg = w * 32 + lane;
+          int blk = -1;
+          if (pg < npages) {
+            blk = bt_row[page0 + pg];
+            if (blk < 0 || blk >= p.NB) {
+              atomicOr(ptr.err, kErrPage);
+              blk = 0;
+            }
+          }
+          return blk;
+        };
+        int cur = fetch(0), nxt = fetch(1);
+        int cur_w = 0;
+        for (int j = 0; j < I.ntiles; ++j, ++g) {
+          const int first = j * ppt;  // page of this tile, relative to the piece
+          if (first / 32 != cur_w) {
+            cur = nxt;
+            cur_w = first / 32;
+            nxt = fetch(cur_w + 1);
+          }
+          const int tile_pages = min(ppt, npages - first);
+          const int mine = tile_pages > pi ? (tile_pages - pi + kProdPerOp - 1) / kProdPerOp : 0;
+          const uint32_t st = g % nst, ph = (g / nst) & 1;
+          int ok = 1;
+          if (lane == 0) {
+            ok = mbar_wait(bar(empty[st]), ph ^ 1, abort_flag, ptr.err);
+            if (ok) mbar_expect_tx(bar(full[st]), (uint32_t)mine * p.P * 128u * 2u);
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) {
+            stop = true;
+            break;
+          }
+          for (int pg = pi; pg < tile_pages; pg += kProdPerOp) {
+            const int blk = __shfl_sync(0xffffffffu, cur, (first + pg) & 31);
+            if (lane == 0) {
+              const uint32_t row = (uint32_t)pg * p.P * 128u;
+              for (int h = 0; h < 2; ++h)
+                tma_load_4d(region + st * kKVTile + h * kKVHalf + row, tmap, h * 128, I.kvh, 0, blk, bar(full[st]),
+                            policy);
+            }
+          }
+          issued[st] = g / nst + 1;
+        }
+      }
+      // Every issued copy has landed before the CTA may exit.
+      if (lane == 0) {
+        for (int s = 0; s < nst; ++s)
+          if (issued[s]) mbar_wait(bar(full[s]), (issued[s] - 1) & 1, abort_flag, ptr.err);
+      }
+      __syncwarp();
+    } else if (warp == 0 || warp == 1) {
+      // ------------------------------------------------------------ MMA issuers
+      // One thread cannot issue tcgen05.mma faster than about one per 44 ns, below the tensor
+      // pipe's rate for these shapes, so S = K Q^T and O^T += V^T P^T come from two warps:
+      // S runs ahead as soon as a K tile and an S buffer are free, P.V as soon as P is
+      // published. The two streams share no operand or accumulator.
+      if (lane == 0) {
+        const bool is_s = warp == 0;
+        uint32_t g = 0;
+        int ii = 0;
+        bool ok = true;
+        for (int it = item_begin; it < item_end && ok; ++it, ++ii) {
+          const Item I = load_item(cp, ptr, it);
+          for (int j = 0; j < I.ntiles && ok; ++j, ++g) {
+            if (is_s) {
+              if (j == 0 && !(ok = mbar_wait(bar(ms.q_full), ii & 1, abort_flag, ptr.err))) break;
+              const uint32_t st = g % kKStages, b = g & 1;
+              if (!(ok = mbar_wait(bar(ms.k_full[st]), (g / kKStages) & 1, abort_flag, ptr.err))) break;
+              if (g >= 2 && !(ok = mbar_wait(bar(ms.s_free[b]), ((g >> 1) - 1) & 1, abort_flag, ptr.err))) break;
+              tc_fence_after();
+              const uint64_t a0 = smem_desc(sbase + kOffK + st * kKVTile, 16, 1024, kSw128);
+              const uint64_t b0 = smem_desc(sbase + kOffQ, 16, 1024, kSw128);
+#pragma unroll
+              for (int kb = 0; kb < 8; ++kb) {
+                const uint32_t off = (kb >> 2) * kKVHalf + (kb & 3) * 32, qoff = (kb >> 2) * kQHalf + (kb & 3) * 32;
+                mma_e4m3(tmem + kColS + b * 128, a0 + (off >> 4), b0 + (qoff >> 4), kIdescS, kb ? 1u : 0u);
+              }
+              mma_commit(bar(ms.s_full[b]));
+              mma_commit(bar(ms.k_empty[st]));
+              if (j == I.ntiles - 1) mma_commit(bar(ms.q_free));
+            } else {
+              // the first P.V of an item overwrites O^T: the previous epilogue must be done
+              if (j == 0 && ii >= 1 && !(ok = mbar_wait(bar(ms.o_free), (ii - 1) & 1, abort_flag, ptr.err))) break;
+              if (!(ok = mbar_wait(bar(ms.p_full), g & 1, abort_flag, ptr.err))) break;
+              const uint32_t st = g % kVStages;
+              if (!(ok = mbar_wait(bar(ms.v_full[st]), (g / kVStages) & 1, abort_flag, ptr.err))) break;
+              tc_fence_after();
+              const uint64_t a0 = smem_desc(sbase + kOffV + st * kKVTile, 1024, 1024, kSw128);
+              const uint64_t b0 = smem_desc(sbase + kOffP, 1024, 1024, kSw128);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint32_t off = h * kKVHalf + kk * 4096, poff = kk * 4096;
+                  mma_e4m3(tmem + kColO + h * 128, a0 + (off >> 4), b0 + (poff >> 4), kIdescO,
+                           (j == 0 && kk == 0) ? 0u : 1u);
+                }
+              }
+              mma_commit(bar(ms.v_empty[st]));
+              mma_commit(bar(ms.p_free));
+              if (j == I.ntiles - 1) mma_commit(bar(ms.o_ready));
+            }
+          }
+        }
+        // Every MMA this thread issued has completed before the CTA may release TMEM.
+        uint64_t& drain = is_s ? ms.drain[0] : ms.drain[1];
+        mma_commit(bar(drain));
+        mbar_wait(bar(drain), 0, abort_flag, ptr.err);
+      }
+      __syncwarp();
+    }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -729,6 +751,17 @@ int launch_verify_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp,
     if (e != cudaSuccess) {
       char buf[160];
       snprintf(buf, sizeof buf, "cudaFuncSetAttribute(verify): %s", cudaGetErrorString(e));
+      set_tc_error(buf);
+      return -1;
+    }
+    // setmaxnreg.inc waits until the registers it asks for are free; the split adds up only
+    // if the kernel starts with exactly kLaunchRegs per thread, so never launch otherwise.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess || fa.numRegs != kLaunchRegs) {
+      char buf[160];
+      snprintf(buf, sizeof buf, "verify kernel built with %d registers per thread; its warpgroup split needs %d",
+               e == cudaSuccess ? fa.numRegs : -1, kLaunchRegs);
       set_tc_error(buf);
       return -1;
     }
