@@ -91,7 +91,9 @@ __device__ inline void finish_split_block(const Problem& p, const Pointers& ptr,
         sum += w;
       }
       const float inv = sum > 0.f ? 1.f / sum : 0.f;
-      for (int i = 0; i < ns; ++i) s_w[i * kSlotRows + r] = lse[i] * inv;
+#pragma unroll
+      for (int i = 0; i < kMergeMaxSplits; ++i)  // static indices keep lse[] in registers
+        if (i < ns) s_w[i * kSlotRows + r] = lse[i] * inv;
     }
     named_barrier(bar_id, nthreads);
 #pragma unroll 4

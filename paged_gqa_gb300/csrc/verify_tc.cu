@@ -59,11 +59,11 @@ constexpr int kSoftWarps = 8;
 constexpr int kSoftThreads = kSoftWarps * 32;
 // 16 warps in four warpgroups. Warpgroup 0: warp 0 = S issuer (+ TMEM owner), warp 1 =
 // P.V issuer, warps 2-3 = K producers; warpgroups 1-2 (warps 4-11) = softmax; warpgroup 3:
-// warp 12 = K producer, warps 13-15 = V producers. The softmax warpgroups take 192
-// registers per thread, the others 64 (setmaxnreg): 2 x 128 x 192 + 2 x 128 x 64 = 65536.
+// warp 12 = K producer, warps 13-15 = V producers. The softmax warpgroups take 184
+// registers per thread, the others 72 (setmaxnreg): 2 x 128 x 184 + 2 x 128 x 72 = 65536.
 constexpr int kVThreads = 512;
 constexpr int kLaunchRegs = 65536 / kVThreads;  // 128: what the split above redistributes
-constexpr int kSoftRegs = 192, kOtherRegs = 64;
+constexpr int kSoftRegs = 184, kOtherRegs = 72;
 static_assert(2 * 128 * kSoftRegs + 2 * 128 * kOtherRegs == kVThreads * kLaunchRegs, "register split");
 constexpr int kSoftWarp0 = 4;
 constexpr int kProdPerOp = 3;  // TMA producer warps per operand (one thread issues too slowly)
@@ -529,33 +529,65 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
       for (int n = 0; n < kCols; ++n) {
         const float lr = ms.red[0][c0 + n] + ms.red[1][c0 + n] + ms.red[2][c0 + n] + ms.red[3][c0 + n];
-        inv[n] = lr > 0.f ? p.out_scale / lr : 0.f;
+        inv[n] = lr > 0.f ? __fdividef(p.out_scale, lr) : 0.f;
       }
       float my_l = 0.f;  // row c0 + lane, for the partial's log-sum-exp
       if (q4 == 0) my_l = ms.red[0][c0 + lane] + ms.red[1][c0 + lane] + ms.red[2][c0 + lane] + ms.red[3][c0 + lane];
       named_barrier(1, kSoftThreads);  // red is reused by the next item's first rescale
       const bool split = I.nsplit > 1;
       const int slot = I.slot_base + I.split;
+      if (split) {
+        // The fp32 partial (64 rows x 256) leaves in 16-row chunks through the P buffer
+        // (free: every P.V of the item has completed) by bulk stores, so these warps do not
+        // wait on thousands of scattered stores; the chunk rows of the slot are contiguous.
+        float* stage = reinterpret_cast<float*>(smem + kOffP);  // 16 rows x 256 floats
+        float* dst0 = slot_o(cp, slot);
+#pragma unroll
+        for (int r0 = 0; r0 < kVN; r0 += 16) {
+          if (r0 >= I.nrows) break;
+          if (c0 == (r0 & 32)) {  // the warps that own rows r0 .. r0+15 (warp-uniform)
+            const int k = r0 & 16;  // compile-time after unrolling: inv[] stays in registers
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < 2; ++h) {
+              float v[16], w[16];
+              tmem_ld16(tmem + lane_addr + kColO + h * 128 + c0 + k, v);
+              tmem_ld16(tmem + lane_addr + kColO + h * 128 + kVN + c0 + k, w);
+              tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < kCols; k += 16) {
-          if (c0 + k < I.nrows) {  // warp-uniform
-            float v[16], w[16];
-            tmem_ld16(tmem + lane_addr + kColO + h * 128 + c0 + k, v);
-            tmem_ld16(tmem + lane_addr + kColO + h * 128 + kVN + c0 + k, w);
-            tmem_wait_ld();
-            const int d = h * 128 + ti;
+              for (int i = 0; i < 16; ++i) stage[i * kHeadDim + h * 128 + ti] = (v[i] + w[i]) * inv[k + i];
+            }
+          }
+          fence_proxy_async_smem();
+          named_barrier(1, kSoftThreads);
+          if (gi == 0) {
+            bulk_store(dst0 + (size_t)r0 * kHeadDim, smem_u32(stage), (uint32_t)min(16, I.nrows - r0) * kHeadDim * 4u);
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+          named_barrier(1, kSoftThreads);
+        }
+        // the partial is in global memory before the block's split counter moves
+        if (gi == 0) {
+          bulk_wait_all();
+          fence_proxy_async_global();
+        }
+      } else {
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int n = c0 + k + i;
-              if (n < I.nrows) {
-                const float val = (v[i] + w[i]) * inv[k + i];
-                if (split) {
-                  slot_o(cp, slot)[(size_t)n * kHeadDim + d] = val;
-                } else {
-                  static_cast<__nv_bfloat16*>(ptr.out)[ms.out_off[pi][n] + d] = __float2bfloat16_rn(val);
-                }
+          for (int k = 0; k < kCols; k += 16) {
+            if (c0 + k < I.nrows) {  // warp-uniform
+              float v[16], w[16];
+              tmem_ld16(tmem + lane_addr + kColO + h * 128 + c0 + k, v);
+              tmem_ld16(tmem + lane_addr + kColO + h * 128 + kVN + c0 + k, w);
+              tmem_wait_ld();
+              const int d = h * 128 + ti;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int n = c0 + k + i;
+                if (n < I.nrows)
+                  static_cast<__nv_bfloat16*>(ptr.out)[ms.out_off[pi][n] + d] =
+                      __float2bfloat16_rn((v[i] + w[i]) * inv[k + i]);
               }
             }
           }
@@ -607,6 +639,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       bool stop = false;
       for (int it = item_begin; it < item_end && !stop; ++it) {
         const Item I = load_item(cp, ptr, it);
+        if (is_k && pi == 0) {
+          // The softmax warps read this item's Q a few tiles from now (this warp runs ahead
+          // by its stages): bring the rows into L2 so that read does not wait on HBM.
+          for (int r = lane; r < I.nrows; r += 32) {
+            const RowMap m = map_row(I.row0 + r, p.G, I.kvh);
+            const uint8_t* row = static_cast<const uint8_t*>(ptr.q) +
+                                 ((size_t)(I.q0 + m.t) * p.q_st + (size_t)m.h * p.q_sh) * (kQFp8 ? 1 : 2);
+#pragma unroll
+            for (int c = 0; c < (kQFp8 ? 256 : 512); c += 128) prefetch_l2(row + c);
+          }
+        }
         const int32_t* bt_row = ptr.block_table + (size_t)I.seq * p.bt_stride;
         const int page0 = I.tile_begin * ppt;                 // first page of the piece
         const int npages = (I.kv_hi + p.P - 1) / p.P - page0; // pages the piece reads
