@@ -8,6 +8,8 @@
 // ("Optimize Qwen3.5 MTP unified attention on gfx950": dispatch gate and segment
 // count chosen from CU parallelism and per-segment KV work; "Tune sparse GQA prefill
 // profile": the >512-program profile branch). Here the split is exact per call.
+#include <cstddef>
+
 #include "common.cuh"
 #include "plan.cuh"
 
@@ -79,34 +81,234 @@ __device__ __forceinline__ long long range_begin(int c, long long U, int C) {
   return (long long)c * U / C;
 }
 
-// Index of the block whose tile range contains unit u (tile_off is non-decreasing).
-__device__ int find_block(const RowBlock* b, int n, long long u) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (b[mid].tile_off <= u) lo = mid; else hi = mid - 1;
+}  // namespace
+
+// Shared-memory caches: sequence info, per-sequence block prefixes and per-block tile
+// counts / offsets for the first kSeqCache sequences and kBlockCache blocks of a class
+// (beyond that, global memory). Later phases read them instead of re-reading what this
+// CTA wrote to global memory, which keeps the plan to a few dependent global accesses.
+constexpr int kSeqCache = 2048;
+constexpr int kBlockCache = 12288;
+constexpr int kMaxCtas = 1024;
+constexpr size_t kPlanSmem = sizeof(int4) * kSeqCache + sizeof(int) * (kSeqCache + 1) +
+                             sizeof(long long) * kBlockCache + sizeof(int) * kBlockCache +
+                             sizeof(int) * (kMaxCtas + 1);
+
+struct PlanSmem {
+  int4* seq;          // q0, qn, L, ok
+  int* seq_pre;       // first block of each cached sequence (class being planned)
+  long long* off;     // tile_off
+  int* tiles;         // tiles
+  int* bfirst;        // first block of CTA range c
+  long long* total;   // scan total
+  int* overflow;
+};
+
+__device__ __forceinline__ SeqInfo seq_of(const Problem& p, const Pointers& ptr, const PlanSmem& sm, int s) {
+  if (s < kSeqCache) {
+    const int4 v = sm.seq[s];
+    return SeqInfo{v.x, v.y, v.z, v.w};
   }
-  return lo;
+  return seq_info(p, ptr, s);
 }
 
-}  // namespace
+// Block i (0-based within sequence s_j, kv heads major) of class cls, written as vectors.
+__device__ __forceinline__ int write_block(const Problem& p, const ClassPlan& cp, int cls, long long bi, int s_j,
+                                          int i, int nb_j, int qn_j, int L_j) {
+  const int rb_rows = cls == 0 ? kVerifyRows : kPrefillRows;
+  const int per_head = nb_j / p.Hkv;
+  const int kvh = i / per_head, rb = i - kvh * per_head;
+  const int row0 = rb * rb_rows;
+  const int nrows = min(rb_rows, qn_j * p.G - row0);
+  const int t_last = (row0 + nrows - 1) / p.G;
+  const int kv_end = L_j - qn_j + t_last + 1;
+  const int tiles = (kv_end + kTileKeys - 1) / kTileKeys;
+  // RowBlocks are 40 bytes: 8-byte aligned, so at most 8-byte vectors
+  int* d = reinterpret_cast<int*>(cp.blocks + bi);
+  static_assert(sizeof(RowBlock) == 40 && offsetof(RowBlock, tile_off) == 24 && alignof(RowBlock) == 8,
+                "RowBlock layout");
+  *reinterpret_cast<int2*>(d) = make_int2(s_j, kvh);
+  *reinterpret_cast<int2*>(d + 2) = make_int2(row0, nrows);
+  *reinterpret_cast<int2*>(d + 4) = make_int2(kv_end, tiles);
+  *reinterpret_cast<long long*>(d + 6) = 0;
+  *reinterpret_cast<int2*>(d + 8) = make_int2(1, 0);
+  return tiles;
+}
+
+__device__ __forceinline__ void plan_class(const Problem& p, const Pointers& ptr, const ClassPlan& cp, int cls,
+                                           const PlanSmem& sm) {
+  auto tiles_of = [&](int b) -> int { return b < kBlockCache ? sm.tiles[b] : cp.blocks[b].tiles; };
+  auto off_of = [&](int b) -> long long { return b < kBlockCache ? sm.off[b] : cp.blocks[b].tile_off; };
+  const int ncached = min(p.num_seqs, kSeqCache);
+  // ---- blocks: per-sequence counts and scan. Cached sequences record their first block
+  // (filled below by all threads at once); the others fill their blocks here, a warp at a
+  // time (one lane per block).
+  long long base = 0;
+  for (int s0 = 0; s0 < p.num_seqs; s0 += blockDim.x) {
+    const int s = s0 + threadIdx.x;
+    SeqInfo si = {0, 0, 0, 0};
+    int nb = 0;
+    if (s < p.num_seqs) {
+      si = seq_of(p, ptr, sm, s);
+      nb = blocks_per_head(si, p.G, cls) * p.Hkv;
+    }
+    const long long pre = block_exclusive_scan(nb, sm.total) + base;
+    if (s < ncached) sm.seq_pre[s] = (int)min(pre, (long long)cp.max_blocks);
+    if (s == ncached - 1) sm.seq_pre[ncached] = (int)min(pre + nb, (long long)cp.max_blocks);
+    if (s0 + (int)blockDim.x > kSeqCache) {
+      const int lane = threadIdx.x & 31;
+      for (int j = 0; j < 32; ++j) {
+        const int nb_j = __shfl_sync(0xffffffffu, nb, j);
+        const long long pre_j = __shfl_sync(0xffffffffu, pre, j);
+        const int qn_j = __shfl_sync(0xffffffffu, si.qn, j);
+        const int L_j = __shfl_sync(0xffffffffu, si.L, j);
+        const int s_j = s0 + (threadIdx.x & ~31) + j;
+        if (nb_j == 0 || s_j < kSeqCache) continue;
+        for (int i = lane; i < nb_j; i += 32) {
+          const long long bi = pre_j + i;
+          if (bi >= cp.max_blocks) {
+            *sm.overflow = 1;
+            break;
+          }
+          const int t = write_block(p, cp, cls, bi, s_j, i, nb_j, qn_j, L_j);
+          if (bi < kBlockCache) sm.tiles[bi] = t;
+        }
+      }
+    }
+    base += *sm.total;
+    __syncthreads();  // the scan total is reused
+  }
+  if (base > cp.max_blocks && threadIdx.x == 0) *sm.overflow = 1;
+  const int nblocks = (int)min(base, (long long)cp.max_blocks);
+  // blocks of cached sequences: every thread a block; its sequence by binary search
+  const int ncb = ncached > 0 ? sm.seq_pre[ncached] : 0;
+  for (int bi = threadIdx.x; bi < ncb; bi += blockDim.x) {
+    int lo = 0, hi = ncached - 1;  // largest s with seq_pre[s] <= bi
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (sm.seq_pre[mid] <= bi) lo = mid; else hi = mid - 1;
+    }
+    const SeqInfo si = seq_of(p, ptr, sm, lo);
+    const int nb_s = blocks_per_head(si, p.G, cls) * p.Hkv;
+    const int t = write_block(p, cp, cls, bi, lo, bi - sm.seq_pre[lo], nb_s, si.qn, si.L);
+    if (bi < kBlockCache) sm.tiles[bi] = t;
+  }
+  __syncthreads();
+
+  // ---- tile prefix over blocks
+  long long tbase = 0;
+  for (int b0 = 0; b0 < nblocks; b0 += blockDim.x) {
+    const int b = b0 + threadIdx.x;
+    const long long t = b < nblocks ? tiles_of(b) : 0;
+    const long long pre = block_exclusive_scan(t, sm.total) + tbase;
+    if (b < nblocks) {
+      cp.blocks[b].tile_off = pre;
+      if (b < kBlockCache) sm.off[b] = pre;
+    }
+    tbase += *sm.total;
+    __syncthreads();
+  }
+  const long long U = tbase;
+  // Cut into at most U ranges so that every range is non-empty: a block then has exactly
+  // one piece per range it intersects, and its split count is exact.
+  const int C = (int)min((long long)cp.num_ctas, U);
+
+  // ---- per-block split count and partial slots; first block of each CTA range
+  int slot_base = 0;
+  for (int b0 = 0; b0 < nblocks; b0 += blockDim.x) {
+    const int b = b0 + threadIdx.x;
+    int ns = 0;
+    if (b < nblocks) {
+      const long long off = off_of(b);
+      const int c_first = cta_of(off, U, C);
+      const int c_last = cta_of(off + tiles_of(b) - 1, U, C);
+      ns = c_last - c_first + 1;
+      cp.counters[b] = 0;
+      // CTA c's range starts inside block b for c in (c_first, c_last], and at its first
+      // tile when the range boundary falls exactly there
+      if (range_begin(c_first, U, C) == off) sm.bfirst[c_first] = b;
+      for (int c = c_first + 1; c <= c_last; ++c) sm.bfirst[c] = b;
+    }
+    const int nslots = ns > 1 ? ns : 0;
+    const long long pre = block_exclusive_scan(nslots, sm.total) + slot_base;
+    if (b < nblocks) {
+      *reinterpret_cast<int2*>(reinterpret_cast<int*>(cp.blocks + b) + 8) = make_int2(ns, (int)pre);
+      if (nslots > 0 && pre + nslots > cp.max_slots) *sm.overflow = 1;
+    }
+    slot_base += (int)*sm.total;
+    __syncthreads();
+  }
+
+  // ---- items: count per CTA, scan, fill
+  long long ibase = 0;
+  for (int c0i = 0; c0i < cp.num_ctas; c0i += blockDim.x) {
+    const int c = c0i + threadIdx.x;
+    int cnt = 0, bfirst = 0;
+    long long u0 = 0, u1 = 0;
+    if (c < C) {
+      u0 = range_begin(c, U, C);
+      u1 = range_begin(c + 1, U, C);
+      bfirst = sm.bfirst[c];
+      int blast = nblocks - 1;
+      if (c + 1 < C) {
+        const int bn = sm.bfirst[c + 1];
+        blast = off_of(bn) == u1 ? bn - 1 : bn;
+      }
+      cnt = blast - bfirst + 1;
+    }
+    const long long pre = block_exclusive_scan(cnt, sm.total) + ibase;
+    if (c < cp.num_ctas) {
+      cp.cta_item_begin[c] = (int)min(pre, (long long)cp.max_items);
+      for (int i = 0; i < cnt; ++i) {
+        const long long ii = pre + i;
+        if (ii >= cp.max_items) {
+          *sm.overflow = 1;
+          break;
+        }
+        const int b = bfirst + i;
+        const long long off = off_of(b);
+        const long long lo = max(u0, off), hi = min(u1, off + tiles_of(b));
+        static_assert(sizeof(WorkItem) == 16, "WorkItem layout");
+        *reinterpret_cast<int4*>(cp.items + ii) =
+            make_int4(b, (int)(lo - off), (int)(hi - off), cta_of(lo, U, C) - cta_of(off, U, C));
+      }
+    }
+    ibase += *sm.total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    cp.cta_item_begin[cp.num_ctas] = (int)min(ibase, (long long)cp.max_items);
+    *cp.n_blocks = nblocks;
+    *cp.n_items = (int)min(ibase, (long long)cp.max_items);
+    *cp.total_tiles = U;
+  }
+  __syncthreads();
+}
 
 __global__ void __launch_bounds__(kPlanThreads, 1)
 plan_kernel(Problem p, Pointers ptr, ClassPlan c0, ClassPlan c1) {
   __shared__ long long s_total;
   __shared__ int s_overflow;
-  ClassPlan plans[2] = {c0, c1};
-  // The attention kernels are launched as programmatic dependents: let them start their
+  extern __shared__ __align__(16) unsigned char plan_smem[];
+  PlanSmem sm;
+  sm.seq = reinterpret_cast<int4*>(plan_smem);
+  sm.off = reinterpret_cast<long long*>(sm.seq + kSeqCache);
+  sm.tiles = reinterpret_cast<int*>(sm.off + kBlockCache);
+  sm.seq_pre = sm.tiles + kBlockCache;
+  sm.bfirst = sm.seq_pre + kSeqCache + 1;
+  sm.total = &s_total;
+  sm.overflow = &s_overflow;
+  // The attention kernels may be launched as programmatic dependents: let them start their
   // prologue now; they wait for this grid's completion before reading the plan.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     s_overflow = 0;
     if (p.num_seqs > 0 && (ptr.qsl[0] != 0 || ptr.qsl[p.num_seqs] != p.T)) atomicOr(ptr.err, kErrBounds);
   }
-
-  // Rows of invalid sequences are zeroed and flagged; they get no blocks.
+  // Sequence info, once. Rows of invalid sequences are zeroed and flagged; they get no blocks.
   for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) {
     SeqInfo si = seq_info(p, ptr, s);
+    if (s < kSeqCache) sm.seq[s] = make_int4(si.q0, si.qn, si.L, si.ok);
     if (!si.ok) {
       atomicOr(ptr.err, kErrBounds);
       int q0 = max(0, si.q0), q1 = min(p.T, max(q0, si.q0 + max(si.qn, 0)));
@@ -116,151 +318,31 @@ plan_kernel(Problem p, Pointers ptr, ClassPlan c0, ClassPlan c1) {
           for (int d = 0; d < kHeadDim; ++d) o[t * p.o_st + h * p.o_sh + d] = 0;
     }
   }
-
-  for (int cls = 0; cls < kNumClasses; ++cls) {
-    ClassPlan& cp = plans[cls];
-    // ---- blocks: per-sequence counts, scan, then fill
-    long long base = 0;
-    for (int s0 = 0; s0 < p.num_seqs; s0 += blockDim.x) {
-      int s = s0 + threadIdx.x;
-      SeqInfo si = {0, 0, 0, 0};
-      int nb = 0;
-      if (s < p.num_seqs) {
-        si = seq_info(p, ptr, s);
-        nb = blocks_per_head(si, p.G, cls) * p.Hkv;
-      }
-      long long pre = block_exclusive_scan(nb, &s_total) + base;
-      // The warp fills the blocks of its 32 sequences together: one lane per block.
-      const int rb_rows = cls == 0 ? kVerifyRows : kPrefillRows;
-      const int lane = threadIdx.x & 31;
-      for (int j = 0; j < 32; ++j) {
-        const int nb_j = __shfl_sync(0xffffffffu, nb, j);
-        if (nb_j == 0) continue;
-        const long long pre_j = __shfl_sync(0xffffffffu, pre, j);
-        const int qn_j = __shfl_sync(0xffffffffu, si.qn, j);
-        const int L_j = __shfl_sync(0xffffffffu, si.L, j);
-        const int s_j = s0 + (threadIdx.x & ~31) + j;
-        const int per_head = nb_j / p.Hkv;
-        const int rows_total = qn_j * p.G;
-        for (int i = lane; i < nb_j; i += 32) {
-          const long long bi = pre_j + i;
-          if (bi >= cp.max_blocks) {
-            s_overflow = 1;
-            break;
-          }
-          const int kvh = i / per_head, rb = i % per_head;
-          RowBlock b;
-          b.seq = s_j;
-          b.kvh = kvh;
-          b.row0 = rb * rb_rows;
-          b.nrows = min(rb_rows, rows_total - b.row0);
-          const int t_last = (b.row0 + b.nrows - 1) / p.G;
-          b.kv_end = L_j - qn_j + t_last + 1;
-          b.tiles = (b.kv_end + kTileKeys - 1) / kTileKeys;
-          b.tile_off = 0;
-          b.nsplit = 1;
-          b.slot_base = 0;
-          cp.blocks[bi] = b;
-        }
-      }
-      base += s_total;
-    }
-    __syncthreads();
-    const int nblocks = (int)min(base, (long long)cp.max_blocks);
-
-    // ---- tile prefix over blocks
-    long long tbase = 0;
-    for (int b0 = 0; b0 < nblocks; b0 += blockDim.x) {
-      int b = b0 + threadIdx.x;
-      long long t = b < nblocks ? cp.blocks[b].tiles : 0;
-      long long pre = block_exclusive_scan(t, &s_total) + tbase;
-      if (b < nblocks) cp.blocks[b].tile_off = pre;
-      tbase += s_total;
-    }
-    __syncthreads();
-    const long long U = tbase;
-    // Cut into at most U ranges so that every range is non-empty: a block then has
-    // exactly one piece per range it intersects, and its split count is exact.
-    const int C = (int)min((long long)cp.num_ctas, U);
-
-    // ---- per-block split count and partial slots
-    int slot_base = 0;
-    for (int b0 = 0; b0 < nblocks; b0 += blockDim.x) {
-      int b = b0 + threadIdx.x;
-      int ns = 0;
-      if (b < nblocks) {
-        RowBlock& rb = cp.blocks[b];
-        int c_first = cta_of(rb.tile_off, U, C);
-        int c_last = cta_of(rb.tile_off + rb.tiles - 1, U, C);
-        rb.nsplit = c_last - c_first + 1;
-        ns = rb.nsplit > 1 ? rb.nsplit : 0;
-        cp.counters[b] = 0;
-      }
-      long long pre = block_exclusive_scan(ns, &s_total) + slot_base;
-      if (b < nblocks) {
-        cp.blocks[b].slot_base = (int)pre;
-        if (ns > 0 && pre + ns > cp.max_slots) s_overflow = 1;
-      }
-      slot_base += (int)s_total;
-    }
-    __syncthreads();
-
-    // ---- items: count per CTA, scan, fill
-    long long ibase = 0;
-    for (int c0i = 0; c0i < cp.num_ctas; c0i += blockDim.x) {
-      int c = c0i + threadIdx.x;
-      int cnt = 0, bfirst = 0;
-      long long u0 = 0, u1 = 0;
-      if (c < C && U > 0) {
-        u0 = range_begin(c, U, C);
-        u1 = range_begin(c + 1, U, C);
-        if (u1 > u0) {
-          bfirst = find_block(cp.blocks, nblocks, u0);
-          int blast = find_block(cp.blocks, nblocks, u1 - 1);
-          cnt = blast - bfirst + 1;
-        }
-      }
-      long long pre = block_exclusive_scan(cnt, &s_total) + ibase;
-      if (c < cp.num_ctas) {
-        cp.cta_item_begin[c] = (int)min(pre, (long long)cp.max_items);
-        for (int i = 0; i < cnt; ++i) {
-          long long ii = pre + i;
-          if (ii >= cp.max_items) { s_overflow = 1; break; }
-          const int b = bfirst + i;
-          const RowBlock& rb = cp.blocks[b];
-          long long lo = max(u0, rb.tile_off), hi = min(u1, rb.tile_off + rb.tiles);
-          WorkItem it;
-          it.block = b;
-          it.tile_begin = (int)(lo - rb.tile_off);
-          it.tile_end = (int)(hi - rb.tile_off);
-          it.split = cta_of(lo, U, C) - cta_of(rb.tile_off, U, C);
-          cp.items[ii] = it;
-        }
-      }
-      ibase += s_total;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      cp.cta_item_begin[cp.num_ctas] = (int)min(ibase, (long long)cp.max_items);
-      *cp.n_blocks = nblocks;
-      *cp.n_items = (int)min(ibase, (long long)cp.max_items);
-      *cp.total_tiles = U;
-    }
-    __syncthreads();
-  }
+  __syncthreads();
+  plan_class(p, ptr, c0, 0, sm);
+  plan_class(p, ptr, c1, 1, sm);
   if (threadIdx.x == 0 && s_overflow) {
     // Host-side bounds make this unreachable; flag it rather than run a partial plan.
     atomicOr(ptr.err, kErrBounds);
-    for (int cls = 0; cls < kNumClasses; ++cls) {
-      *plans[cls].n_items = 0;
-      for (int c = 0; c <= plans[cls].num_ctas; ++c) plans[cls].cta_item_begin[c] = 0;
-    }
+    *c0.n_items = 0;
+    *c1.n_items = 0;
+    for (int c = 0; c <= c0.num_ctas; ++c) c0.cta_item_begin[c] = 0;
+    for (int c = 0; c <= c1.num_ctas; ++c) c1.cta_item_begin[c] = 0;
   }
 }
 
 cudaError_t launch_plan(const Problem& p, const Pointers& ptr, const ClassPlan& v,
                         const ClassPlan& f, cudaStream_t stream) {
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p, ptr, v, f);
+  if (v.num_ctas > kMaxCtas || f.num_ctas > kMaxCtas) return cudaErrorInvalidConfiguration;
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPlanSmem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = 1;
+  }
+  plan_kernel<<<1, kPlanThreads, kPlanSmem, stream>>>(p, ptr, v, f);
   return cudaGetLastError();
 }
 

@@ -159,6 +159,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &ms.abort_flag;
   auto bar = [&](const uint64_t& b) { return smem_u32(&b); };
+  // The plan is read once the previous grid (the plan kernel) has completed. A CTA with no
+  // work (an empty class, or fewer items than CTAs) leaves before any set-up.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int item_begin = cp.cta_item_begin[blockIdx.x];
+  const int item_end = cp.cta_item_begin[blockIdx.x + 1];
+  if (item_begin >= item_end) return;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKStages; ++s) {
@@ -191,11 +197,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
-  // Launched as a programmatic dependent: the prologue above overlaps the previous
-  // kernel; the plan is read only after the previous grids have completed.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int item_begin = cp.cta_item_begin[blockIdx.x];
-  const int item_end = cp.cta_item_begin[blockIdx.x + 1];
+  // The next kernel on the stream (the other class) may start its own checks now.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0 || warp == kVProducerWarp) {

@@ -176,6 +176,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   volatile int* abort_flag = &ms.abort_flag;
 
   auto bar = [&](const uint64_t& b) { return smem_u32(&b); };
+  // The plan is read once the previous grid (the plan kernel) has completed. A CTA with no
+  // work (an empty class, or fewer items than CTAs) leaves before any set-up.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int item_begin = cp.cta_item_begin[blockIdx.x];
+  const int item_end = cp.cta_item_begin[blockIdx.x + 1];
+  if (item_begin >= item_end) return;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKStages; ++s) {
@@ -209,11 +215,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
-  // When launched as a programmatic dependent of the plan kernel, the prologue above
-  // overlaps it; the plan is read only after it has completed.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int item_begin = cp.cta_item_begin[blockIdx.x];
-  const int item_end = cp.cta_item_begin[blockIdx.x + 1];
+  // The next kernel on the stream (the other class) may start its own checks now.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // Warpgroup roles. setmaxnreg is executed by all four warps of a warpgroup, first thing

@@ -82,6 +82,19 @@ def test_many_short_sequences(path):
     gu.check_full(case, gu.run_library(case), "many short")
 
 
+def test_plan_beyond_shared_memory_caches(path):
+    """More sequences (2600) and row blocks (~21000) than the plan kernel keeps in shared
+    memory, with prefill sequences past the cached range: the plan's global-memory paths."""
+    gen = torch.Generator().manual_seed(21)
+    seqs = [(int(q), int(L)) for q, L in zip(torch.randint(1, 5, (2600,), generator=gen),
+                                                torch.randint(4, 160, (2600,), generator=gen))]
+    for i in (5, 2100, 2599):
+        seqs[i] = (40, 300)  # 40 tokens x G=2 = 80 rows: prefill blocks
+    spec = wl.CaseSpec("beyond caches", seqs, 16, 8, 16)
+    case = wl.make_case(spec, device="cuda", seed=21, poison=True)
+    gu.check_full(case, gu.run_library(case), "beyond plan caches")
+
+
 def test_long_single_sequence_is_split(path):
     """One sequence, one kv head: its keys are cut across all CTAs and merged."""
     spec = wl.CaseSpec("long", [(4, 40000)], 16, 1, 16)
