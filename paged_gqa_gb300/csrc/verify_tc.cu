@@ -29,8 +29,8 @@
 //   * persistent CTAs (one per SM) walk a contiguous range of key tiles cut by the plan
 //     kernel; a block cut across CTAs is finished by the last piece with a log-sum-exp merge.
 //
-// Warp roles (512 threads): warp 0 = S issuer (+ TMEM owner), warp 1 = P.V issuer, warps
-// 2, 3, 12 = K producers (TMA), warps 4-11 = softmax and epilogue, warps 13-15 = V
+// Warp roles (768 threads): warp 0 = S issuer (+ TMEM owner), warp 1 = P.V issuer, warps
+// 2, 3, 20 = K producers (TMA), warps 4-19 = softmax and epilogue, warps 21-23 = V
 // producers (TMA). Softmax thread (q, c, lane)
 // owns TMEM lane 32q+lane (= key of the tile, = d within a d-half for O^T) and rows
 // [32c, 32c+32). Shared memory: Q hi/lo 32 KB, 2 K stages and 3 V stages of 32 KB, P hi/lo
@@ -55,19 +55,25 @@ namespace {
 using namespace tc;
 
 constexpr int kVN = 64;            // query rows of a verify block (MMA N per Q or P part)
-constexpr int kSoftWarps = 8;
+constexpr int kSoftWarps = 16;     // four per TMEM lane quarter: the softmax is latency-bound
 constexpr int kSoftThreads = kSoftWarps * 32;
-// 16 warps in four warpgroups. Warpgroup 0: warp 0 = S issuer (+ TMEM owner), warp 1 =
-// P.V issuer, warps 2-3 = K producers; warpgroups 1-2 (warps 4-11) = softmax; warpgroup 3:
-// warp 12 = K producer, warps 13-15 = V producers. The softmax warpgroups take 184
-// registers per thread, the others 72 (setmaxnreg): 2 x 128 x 184 + 2 x 128 x 72 = 65536.
-constexpr int kVThreads = 512;
-constexpr int kLaunchRegs = 65536 / kVThreads;  // 128: what the split above redistributes
-constexpr int kSoftRegs = 184, kOtherRegs = 72;
-static_assert(2 * 128 * kSoftRegs + 2 * 128 * kOtherRegs == kVThreads * kLaunchRegs, "register split");
+constexpr int kRowGroups = kSoftWarps / 4;
+constexpr int kCols = kVN / kRowGroups;  // rows per softmax thread (16)
+// 24 warps in six warpgroups. Warpgroup 0: warp 0 = S issuer (+ TMEM owner), warp 1 = P.V
+// issuer, warps 2-3 = K producers; warpgroups 1-4 (warps 4-19) = softmax; warpgroup 5:
+// warp 20 = K producer, warps 21-23 = V producers. The kernel starts with 80 registers a
+// thread (65536 / 768, rounded down to 8); the softmax warpgroups then take 96 and the
+// others 48 (setmaxnreg): 4 x 128 x 96 + 2 x 128 x 48 = 768 x 80.
+constexpr int kVThreads = 768;
+constexpr int kLaunchRegs = 80;
+constexpr int kSoftRegs = 96, kOtherRegs = 48;
+static_assert(kLaunchRegs == (65536 / kVThreads) / 8 * 8, "launch registers");
+static_assert(4 * 128 * kSoftRegs + 2 * 128 * kOtherRegs == kVThreads * kLaunchRegs, "register split");
+static_assert(kCols == 16, "the epilogue's row-sum reduction assumes 16 rows per thread");
 constexpr int kSoftWarp0 = 4;
+constexpr int kQChunks = kVN * 16 / kSoftThreads;  // Q chunks of 16 elements per softmax thread
+static_assert(kQChunks * kSoftThreads == kVN * 16, "Q chunks");
 constexpr int kProdPerOp = 3;  // TMA producer warps per operand (one thread issues too slowly)
-constexpr int kCols = kVN / 2;     // rows per softmax thread
 constexpr int kKStages = 2;        // K tiles in shared memory (freed by S = K Q^T)
 constexpr int kVStages = 3;        // V tiles in shared memory (held until O += P V)
 constexpr float kTau = 4.f;        // rescale when a score exceeds the reference by 2^kTau
@@ -221,11 +227,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   // Warpgroup roles. setmaxnreg is executed by all four warps of a warpgroup, first thing
   // in its role's branch (the launcher checks that the kernel starts with kLaunchRegs).
   const int wg = warp >> 2;
-  if (wg == 1 || wg == 2) {
+  if (wg >= 1 && wg <= kRowGroups) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftRegs));
     // ------------------------------------------------------------ softmax + epilogue
-    const int sw = warp - kSoftWarp0;        // 0..7
-    const int gi = sw * 32 + lane;           // 0..255
+    const int sw = warp - kSoftWarp0;        // 0..15
+    const int gi = sw * 32 + lane;           // 0..511
     const int q4 = warp & 3;                 // TMEM lane quarter
     const int c0 = (sw >> 2) * kCols;        // first row (column) this thread owns
     const int ti = q4 * 32 + lane;           // TMEM lane = key in tile = d in half
@@ -252,7 +258,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         ms.m[pi][n] = n < I.nrows ? kMInit : 0.f;
         ms.mo[pi][n] = kSigma - ms.m[pi][n];
       }
-      // 64 rows x 16 chunks of 16 elements; thread gi takes chunks gi + 256k, k < 4
+      // 64 rows x 16 chunks of 16 elements; thread gi takes chunks gi + kSoftThreads k
       auto src_of = [&](int r, int ch) -> const uint8_t* {
         const RowMap m = map_row(I.row0 + r, p.G, I.kvh);
         return static_cast<const uint8_t*>(ptr.q) +
@@ -264,23 +270,23 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         return smem + kOffQ + h * kQHalf + rr * 128 + ((c ^ (rr & 7)) << 4);
       };
       if (kQFp8) {
-        uint4 v[4];
+        uint4 v[kQChunks];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kQChunks; ++k) {
           const int c = gi + k * kSoftThreads, r = c >> 4, ch = c & 15;
           v[k] = r < I.nrows ? *reinterpret_cast<const uint4*>(src_of(r, ch)) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kQChunks; ++k) {
           const int c = gi + k * kSoftThreads, r = c >> 4, ch = c & 15;
           *reinterpret_cast<uint4*>(dst_of(0, r, ch)) = v[k];
         }
         if (gi == 0) ms.qscale[pi] = 1.f;
       } else {
-        uint4 v[4][2];
+        uint4 v[kQChunks][2];
         float amax = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kQChunks; ++k) {
           const int c = gi + k * kSoftThreads, r = c >> 4, ch = c & 15;
           if (r < I.nrows) {
             const uint4* s = reinterpret_cast<const uint4*>(src_of(r, ch));
@@ -291,7 +297,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           }
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kQChunks; ++k) {
           const uint32_t w[8] = {v[k][0].x, v[k][0].y, v[k][0].z, v[k][0].w,
                                  v[k][1].x, v[k][1].y, v[k][1].z, v[k][1].w};
 #pragma unroll
@@ -312,7 +318,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         sig = max(-100, min(100, sig));
         const float scale = ldexpf(1.f, sig);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kQChunks; ++k) {
           const int c = gi + k * kSoftThreads, r = c >> 4, ch = c & 15;
           const uint32_t w[8] = {v[k][0].x, v[k][0].y, v[k][0].z, v[k][0].w,
                                  v[k][1].x, v[k][1].y, v[k][1].z, v[k][1].w};
@@ -479,17 +485,19 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           if (!mbar_wait(bar(ms.v_full[st]), (g / kVStages) & 1, abort_flag, ptr.err)) bad = true;
           if (key >= I.kv_hi) {
             const uint4 z = make_uint4(0, 0, 0, 0);
-            // this thread zeroes its row's d-half (c0 == 0 -> d 0..127, else 128..255)
-            uint4* row = reinterpret_cast<uint4*>(smem + kOffV + st * kKVTile + (c0 ? kKVHalf : 0) + ti * 128);
+            // the kRowGroups threads of key ti zero 64 bytes each: d-half rg / 2, 16-byte
+            // chunks 4 (rg % 2) .. 4 (rg % 2) + 3 of the (swizzled) 128-byte row
+            const int rg = c0 / kCols;
+            uint8_t* row = smem + kOffV + st * kKVTile + (rg >> 1) * kKVHalf + ti * 128;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) row[i] = z;
+            for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(row + ((((rg & 1) * 4 + i) ^ (ti & 7)) << 4)) = z;
           }
         }
         // P^T row of key ti: [P_hi rows 0..63 | P_lo rows 0..63], 128-byte swizzle; this
-        // thread writes rows [c0, c0+32) of both parts
+        // thread writes rows [c0, c0 + kCols) of both parts
         {
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
+          for (int cc = 0; cc < kCols / 16; ++cc) {
             const int chunk_hi = (c0 >> 4) + cc, chunk_lo = 4 + chunk_hi;
             *reinterpret_cast<uint4*>(smem + kOffP + ti * 128 + ((chunk_hi ^ (ti & 7)) << 4)) =
                 make_uint4(ph[4 * cc], ph[4 * cc + 1], ph[4 * cc + 2], ph[4 * cc + 3]);
@@ -514,7 +522,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
         for (int n = 0; n < kCols; ++n) v[n] = l[n];
 #pragma unroll
-        for (int w = 16, o = 16; o >= 1; w >>= 1, o >>= 1) {
+        for (int w = kCols / 2, o = 16; o >= 2; w >>= 1, o >>= 1) {
           const bool up = lane & o;
 #pragma unroll
           for (int i = 0; i < w; ++i) {
@@ -523,8 +531,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
           }
         }
-        // lane now holds row c0 + lane
-        ms.red[q4][c0 + lane] = v[0];
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+        // lanes 2r and 2r+1 now hold row c0 + r
+        if ((lane & 1) == 0) ms.red[q4][c0 + (lane >> 1)] = v[0];
       }
       named_barrier(1, kSoftThreads);
       float inv[kCols];
@@ -533,8 +542,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         const float lr = ms.red[0][c0 + n] + ms.red[1][c0 + n] + ms.red[2][c0 + n] + ms.red[3][c0 + n];
         inv[n] = lr > 0.f ? __fdividef(p.out_scale, lr) : 0.f;
       }
-      float my_l = 0.f;  // row c0 + lane, for the partial's log-sum-exp
-      if (q4 == 0) my_l = ms.red[0][c0 + lane] + ms.red[1][c0 + lane] + ms.red[2][c0 + lane] + ms.red[3][c0 + lane];
+      float my_l = 0.f;  // row c0 + lane (lane < kCols), for the partial's log-sum-exp
+      if (q4 == 0 && lane < kCols)
+        my_l = ms.red[0][c0 + lane] + ms.red[1][c0 + lane] + ms.red[2][c0 + lane] + ms.red[3][c0 + lane];
       named_barrier(1, kSoftThreads);  // red is reused by the next item's first rescale
       const bool split = I.nsplit > 1;
       const int slot = I.slot_base + I.split;
@@ -547,8 +557,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
         for (int r0 = 0; r0 < kVN; r0 += 16) {
           if (r0 >= I.nrows) break;
-          if (c0 == (r0 & 32)) {  // the warps that own rows r0 .. r0+15 (warp-uniform)
-            const int k = r0 & 16;  // compile-time after unrolling: inv[] stays in registers
+          if (c0 == r0 - r0 % kCols) {  // the warps that own rows r0 .. r0+15 (warp-uniform)
+            const int k = r0 % kCols;  // compile-time after unrolling: inv[] stays in registers
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
               float v[16], w[16];
@@ -598,7 +608,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       tc_fence_before();
       mbar_arrive(bar(ms.o_free));
       if (split) {
-        if (q4 == 0 && c0 + lane < I.nrows) {
+        if (q4 == 0 && lane < kCols && c0 + lane < I.nrows) {
           const int row = c0 + lane;
           slot_lse(cp, slot)[row] = my_l > 0.f ? ms.m[pi][row] - kSigma + log2f(my_l) : -INFINITY;
         }
@@ -617,8 +627,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
-    const bool k_prod = warp == 2 || warp == 3 || warp == 12;
-    const bool v_prod = warp >= 13;
+    const bool k_prod = warp == 2 || warp == 3 || warp == 20;
+    const bool v_prod = warp >= 21;
     if (k_prod || v_prod) {
       // ------------------------------------------------------------ TMA producers (K, V)
       // K and V have their own warps, so K tiles run ahead as soon as S = K Q^T frees a
@@ -627,7 +637,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       // d-halves back to back), since one thread issues page-sized boxes too slowly to keep
       // HBM busy.
       const bool is_k = k_prod;
-      const int pi = is_k ? (warp == 12 ? 2 : warp - 2) : warp - 13;
+      const int pi = is_k ? (warp == 20 ? 2 : warp - 2) : warp - 21;
       const CUtensorMap* tmap = is_k ? &tmap_k : &tmap_v;
       const int nst = is_k ? kKStages : kVStages;
       const uint32_t region = sbase + (is_k ? kOffK : kOffV);
