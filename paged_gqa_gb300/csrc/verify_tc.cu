@@ -234,6 +234,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     const int gi = sw * 32 + lane;           // 0..511
     const int q4 = warp & 3;                 // TMEM lane quarter
     const int c0 = (sw >> 2) * kCols;        // first row (column) this thread owns
+    const int group_bar = 3 + (sw >> 2);     // named barrier of the row group's four warps
     const int ti = q4 * 32 + lane;           // TMEM lane = key in tile = d in half
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
     float l[kCols];
@@ -362,7 +363,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       named_barrier(1, kSoftThreads);  // q_prep's shared writes (lim, m, qscale) are visible
       const float c = p.score_scale_log2 * ms.qscale[pi];
       const int min_lim = I.L - I.qn + map_row(I.row0, p.G, I.kvh).t;
-      bool aborted = false;
+      // A failed wait (timeout or abort) does not leave the loops: every later wait then
+      // fails fast, so all softmax warps still pass the same barriers and finish.
       for (int j = 0; j < I.ntiles; ++j, ++g) {
         const int b = g & 1;
         const int key0 = (I.tile_begin + j) * kTileKeys;
@@ -398,18 +400,16 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             xmax = fmaxf(xmax, fmaxf(fmaxf(t[n], t[n + 1]), fmaxf(t[n + 2], t[n + 3])));
           }
         }
-        // vote: does any score exceed its row reference by more than 2^kTau?
+        // vote of the row group (its four warps hold all 128 keys of its rows): does any
+        // score exceed its row reference by more than 2^kTau? Row groups do not wait for
+        // one another, so their phases interleave.
         const bool mine = xmax > kTau + kSigma;
-        const int wv = (__any_sync(0xffffffffu, mine) ? 1 : 0) | ((bad || *abort_flag) ? 2 : 0);
+        const int wv = __any_sync(0xffffffffu, mine) ? 1 : 0;
         if (lane == 0) ms.vote[g & 1][sw] = wv;
-        named_barrier(1, kSoftThreads);
+        named_barrier(group_bar, 128);
         int votes = 0;
 #pragma unroll
-        for (int w = 0; w < kSoftWarps; ++w) votes |= ms.vote[g & 1][w];
-        if (votes & 2) {
-          aborted = true;
-          break;
-        }
+        for (int w = 0; w < 4; ++w) votes |= ms.vote[g & 1][(sw & ~3) + w];
         const bool rescale = votes & 1;
         if (rescale) {
           // Reload the raw scores (S buffer b is released only after this block; x may have
@@ -426,9 +426,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             const float r = warp_max(t[n]);
             if (lane == n) ms.red[q4][c0 + n] = r;
           }
-          named_barrier(1, kSoftThreads);
-          if (gi < kVN) {
-            const int n = gi;
+          named_barrier(group_bar, 128);
+          if (q4 == 0 && lane < kCols) {
+            const int n = c0 + lane;
             const float mt = fmaxf(fmaxf(ms.red[0][n], ms.red[1][n]), fmaxf(ms.red[2][n], ms.red[3][n]));
             const float m_old = ms.m[pi][n];
             const float mn = fmaxf(m_old, mt);
@@ -436,7 +436,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             ms.m[pi][n] = mn;
             ms.mo[pi][n] = kSigma - mn;
           }
-          named_barrier(1, kSoftThreads);
+          named_barrier(group_bar, 128);
 #pragma unroll
           for (int n = 0; n < kCols; ++n) {
             t[n] += ms.mo[pi][c0 + n];
@@ -509,7 +509,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         tc_fence_before();
         mbar_arrive(bar(ms.p_full));
       }
-      if (aborted) break;
       // Q of the next item while this item's last P.V runs
       if (it + 1 < item_end) q_prep(load_item(cp, ptr, it + 1), ii + 1);
 
