@@ -38,7 +38,7 @@ struct RowBlock {
   int row0, nrows;      // rows [row0, row0 + nrows) of the (seq, kvh) row space
   int kv_end;           // keys [0, kv_end) are visible to the block's last row
   int tiles;            // ceil(kv_end / kTileKeys)
-  long long tile_off;   // exclusive prefix of tiles within the class
+  long long tile_off;   // plan only: first unit of the block's span (fixed cost, then tiles)
   int nsplit;           // number of pieces (CTAs) the block is cut into
   int slot_base;        // first partial slot (valid when nsplit > 1)
 };

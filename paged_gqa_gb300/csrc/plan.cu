@@ -90,6 +90,9 @@ __device__ __forceinline__ long long range_begin(int c, long long U, int C) {
 constexpr int kSeqCache = 2048;
 constexpr int kBlockCache = 12288;
 constexpr int kMaxCtas = 1024;
+// What starting a row block costs a CTA, in key tiles (Q load, epilogue, merge): measured
+// about 8 us at ~1.6 us per tile for verify blocks; prefill blocks have longer tiles.
+__host__ __device__ constexpr int fixed_cost(int cls) { return cls == 0 ? 5 : 2; }
 constexpr size_t kPlanSmem = sizeof(int4) * kSeqCache + sizeof(int) * (kSeqCache + 1) +
                              sizeof(long long) * kBlockCache + sizeof(int) * kBlockCache +
                              sizeof(int) * (kMaxCtas + 1);
@@ -195,11 +198,14 @@ __device__ __forceinline__ void plan_class(const Problem& p, const Pointers& ptr
   }
   __syncthreads();
 
-  // ---- tile prefix over blocks
+  // ---- unit prefix over blocks. A block spans fixed_cost(cls) units for what starting it
+  // costs a CTA (loading Q, the epilogue, a merge) and then one unit per key tile; the
+  // units are cut into equal CTA ranges, so a CTA that starts blocks gets fewer tiles.
+  const int E = fixed_cost(cls);
   long long tbase = 0;
   for (int b0 = 0; b0 < nblocks; b0 += blockDim.x) {
     const int b = b0 + threadIdx.x;
-    const long long t = b < nblocks ? tiles_of(b) : 0;
+    const long long t = b < nblocks ? tiles_of(b) + E : 0;
     const long long pre = block_exclusive_scan(t, sm.total) + tbase;
     if (b < nblocks) {
       cp.blocks[b].tile_off = pre;
@@ -209,24 +215,23 @@ __device__ __forceinline__ void plan_class(const Problem& p, const Pointers& ptr
     __syncthreads();
   }
   const long long U = tbase;
-  // Cut into at most U ranges so that every range is non-empty: a block then has exactly
-  // one piece per range it intersects, and its split count is exact.
+  // At most U ranges, none empty in units (a range may hold no tile: that CTA has no item).
   const int C = (int)min((long long)cp.num_ctas, U);
 
-  // ---- per-block split count and partial slots; first block of each CTA range
+  // ---- per-block split count and partial slots; block containing the start of each range
   int slot_base = 0;
   for (int b0 = 0; b0 < nblocks; b0 += blockDim.x) {
     const int b = b0 + threadIdx.x;
     int ns = 0;
     if (b < nblocks) {
-      const long long off = off_of(b);
-      const int c_first = cta_of(off, U, C);
-      const int c_last = cta_of(off + tiles_of(b) - 1, U, C);
-      ns = c_last - c_first + 1;
+      const long long span = off_of(b), real = span + E;  // tiles occupy [real, real + tiles)
+      const int tiles = tiles_of(b);
+      ns = cta_of(real + tiles - 1, U, C) - cta_of(real, U, C) + 1;  // pieces: ranges meeting the tiles
       cp.counters[b] = 0;
-      // CTA c's range starts inside block b for c in (c_first, c_last], and at its first
-      // tile when the range boundary falls exactly there
-      if (range_begin(c_first, U, C) == off) sm.bfirst[c_first] = b;
+      // CTA c's range starts inside block b's span for c in (c_first, c_last], and at its
+      // first unit when the range boundary falls exactly there
+      const int c_first = cta_of(span, U, C), c_last = cta_of(span + E + tiles - 1, U, C);
+      if (range_begin(c_first, U, C) == span) sm.bfirst[c_first] = b;
       for (int c = c_first + 1; c <= c_last; ++c) sm.bfirst[c] = b;
     }
     const int nslots = ns > 1 ? ns : 0;
@@ -239,7 +244,9 @@ __device__ __forceinline__ void plan_class(const Problem& p, const Pointers& ptr
     __syncthreads();
   }
 
-  // ---- items: count per CTA, scan, fill
+  // ---- items: count per CTA, scan, fill. The items of range [u0, u1) are the blocks whose
+  // tiles meet it: from the block whose span holds u0 to the block whose span holds
+  // u1 - 1, less that last one if u1 - 1 falls in its fixed-cost units.
   long long ibase = 0;
   for (int c0i = 0; c0i < cp.num_ctas; c0i += blockDim.x) {
     const int c = c0i + threadIdx.x;
@@ -254,7 +261,8 @@ __device__ __forceinline__ void plan_class(const Problem& p, const Pointers& ptr
         const int bn = sm.bfirst[c + 1];
         blast = off_of(bn) == u1 ? bn - 1 : bn;
       }
-      cnt = blast - bfirst + 1;
+      if (u1 - 1 < off_of(blast) + E) --blast;
+      cnt = max(0, blast - bfirst + 1);
     }
     const long long pre = block_exclusive_scan(cnt, sm.total) + ibase;
     if (c < cp.num_ctas) {
@@ -266,11 +274,11 @@ __device__ __forceinline__ void plan_class(const Problem& p, const Pointers& ptr
           break;
         }
         const int b = bfirst + i;
-        const long long off = off_of(b);
-        const long long lo = max(u0, off), hi = min(u1, off + tiles_of(b));
+        const long long real = off_of(b) + E;
+        const long long lo = max(u0, real), hi = min(u1, real + tiles_of(b));
         static_assert(sizeof(WorkItem) == 16, "WorkItem layout");
         *reinterpret_cast<int4*>(cp.items + ii) =
-            make_int4(b, (int)(lo - off), (int)(hi - off), cta_of(lo, U, C) - cta_of(off, U, C));
+            make_int4(b, (int)(lo - real), (int)(hi - real), cta_of(lo, U, C) - cta_of(real, U, C));
       }
     }
     ibase += *sm.total;
