@@ -40,6 +40,17 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier that also returns whether `pred` holds for any participating thread.
+__device__ __forceinline__ bool barrier_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // Partial result slot of (block, split).
 __device__ __forceinline__ float* slot_o(const ClassPlan& cp, int slot) {
   return cp.part_o + (size_t)slot * cp.slot_rows * kHeadDim;

@@ -118,7 +118,6 @@ struct Misc {
   float amax[kSoftWarps];
   uint32_t tmem_base;
   int abort_flag;
-  int vote[2][kSoftWarps];
   int merge_flag;
 };
 static_assert(offsetof(Misc, m) % 16 == 0 && offsetof(Misc, k_full) % 8 == 0, "Misc alignment");
@@ -403,14 +402,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         // vote of the row group (its four warps hold all 128 keys of its rows): does any
         // score exceed its row reference by more than 2^kTau? Row groups do not wait for
         // one another, so their phases interleave.
-        const bool mine = xmax > kTau + kSigma;
-        const int wv = __any_sync(0xffffffffu, mine) ? 1 : 0;
-        if (lane == 0) ms.vote[g & 1][sw] = wv;
-        named_barrier(group_bar, 128);
-        int votes = 0;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) votes |= ms.vote[g & 1][(sw & ~3) + w];
-        const bool rescale = votes & 1;
+        const bool rescale = barrier_or(group_bar, 128, xmax > kTau + kSigma);
         if (rescale) {
           // Reload the raw scores (S buffer b is released only after this block; x may have
           // lost s entirely against a -1e30 reference), take the exact tile maximum of s c
