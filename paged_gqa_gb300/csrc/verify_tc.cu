@@ -31,11 +31,10 @@
 //
 // Warp roles (768 threads): warp 0 = S issuer (+ TMEM owner), warp 1 = P.V issuer, warps
 // 2, 3, 20 = K producers (TMA), warps 4-19 = softmax and epilogue, warps 21-23 = V
-// producers (TMA). Softmax thread (q, c, lane)
-// owns TMEM lane 32q+lane (= key of the tile, = d within a d-half for O^T) and rows
-// [32c, 32c+32). Shared memory: Q hi/lo 32 KB, 2 K stages and 3 V stages of 32 KB, P hi/lo
-// 16 KB, barriers and row state (~221 KB, one CTA per SM). TMEM: 2 S buffers of 128
-// columns, O^T 256 columns.
+// producers (TMA). Softmax thread (q, c, lane) owns TMEM lane 32q+lane (= key of the tile,
+// = d within a d-half for O^T) and rows [16c, 16c+16). Shared memory: Q hi/lo 32 KB, 2 K
+// and 2 V stages of 32 KB, two P hi/lo buffers of 16 KB, barriers and row state (~205 KB,
+// one CTA per SM). TMEM: 2 S buffers of 128 columns, O^T 256 columns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -75,7 +74,8 @@ constexpr int kQChunks = kVN * 16 / kSoftThreads;  // Q chunks of 16 elements pe
 static_assert(kQChunks * kSoftThreads == kVN * 16, "Q chunks");
 constexpr int kProdPerOp = 3;  // TMA producer warps per operand (one thread issues too slowly)
 constexpr int kKStages = 2;        // K tiles in shared memory (freed by S = K Q^T)
-constexpr int kVStages = 3;        // V tiles in shared memory (held until O += P V)
+constexpr int kVStages = 2;        // V tiles in shared memory (held until O += P V)
+constexpr int kPBufs = 2;          // P buffers: P(g+1) is written while P.V(g) runs
 constexpr float kTau = 4.f;        // rescale when a score exceeds the reference by 2^kTau
 constexpr float kSigma = 4.f;      // P is stored scaled by 2^kSigma (max 2^(kTau+kSigma) = 256)
 constexpr float kMInit = -1.0e30f; // reference of a row before its first key
@@ -89,7 +89,8 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + 2 * kQHalf;
 constexpr uint32_t kOffV = kOffK + kKStages * kKVTile;
 constexpr uint32_t kOffP = kOffV + kVStages * kKVTile;  // [128 keys][P_hi 64 B | P_lo 64 B]
-constexpr uint32_t kOffMisc = kOffP + kTileKeys * 128;
+constexpr uint32_t kPBuf = kTileKeys * 128;  // 16 KB
+constexpr uint32_t kOffMisc = kOffP + kPBufs * kPBuf;
 
 // TMEM columns: S buffers [S_hi | S_lo] (2 x 128), O^T d-half h [O_hi | O_lo] (2 x 128).
 constexpr uint32_t kTmemCols = 512;
@@ -113,7 +114,7 @@ struct Misc {
   alignas(16) float merge_w[kMergeMaxSplits * kSlotRows];
   alignas(8) uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], s_free[2];
-  uint64_t p_full, p_free, q_full, q_free, o_ready, o_free, drain[2];
+  uint64_t p_full[kPBufs], pv_done[kPBufs], q_full, q_free, o_ready, o_free, drain[2];
   float qscale[2];
   float amax[kSoftWarps];
   uint32_t tmem_base;
@@ -201,8 +202,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       mbar_init(bar(ms.s_full[b]), 1);
       mbar_init(bar(ms.s_free[b]), kSoftThreads);
     }
-    mbar_init(bar(ms.p_full), kSoftThreads);
-    mbar_init(bar(ms.p_free), 1);
+    for (int b = 0; b < kPBufs; ++b) {
+      mbar_init(bar(ms.p_full[b]), kSoftThreads);
+      mbar_init(bar(ms.pv_done[b]), 1);
+    }
     mbar_init(bar(ms.q_full), kSoftThreads);
     mbar_init(bar(ms.q_free), 1);
     mbar_init(bar(ms.o_ready), 1);
@@ -451,8 +454,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           l[n + 2] += f23.x;
           l[n + 3] += f23.y;
         }
-        // P buffer and O^T are free once the previous tile's P.V has completed
-        if (g >= 1 && !mbar_wait(bar(ms.p_free), (g - 1) & 1, abort_flag, ptr.err)) bad = true;
+        // P buffer g & 1 is free once P.V(g-2) has completed; O^T may be rescaled once
+        // P.V(g-1) has. Each barrier's next phase needs a P these threads have not written yet,
+        // so a late parity wait cannot mistake it for the phase it waits for.
+        if (g >= 2 && !mbar_wait(bar(ms.pv_done[g & 1]), ((g >> 1) - 1) & 1, abort_flag, ptr.err)) bad = true;
+        if (rescale && j > 0 && !mbar_wait(bar(ms.pv_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, abort_flag, ptr.err))
+          bad = true;
         tc_fence_after();
         if (rescale && j > 0) {
           // O^T (both d-halves, both P parts), column by column
@@ -491,15 +498,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
           for (int cc = 0; cc < kCols / 16; ++cc) {
             const int chunk_hi = (c0 >> 4) + cc, chunk_lo = 4 + chunk_hi;
-            *reinterpret_cast<uint4*>(smem + kOffP + ti * 128 + ((chunk_hi ^ (ti & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(smem + kOffP + (g & 1) * kPBuf + ti * 128 + ((chunk_hi ^ (ti & 7)) << 4)) =
                 make_uint4(ph[4 * cc], ph[4 * cc + 1], ph[4 * cc + 2], ph[4 * cc + 3]);
-            *reinterpret_cast<uint4*>(smem + kOffP + ti * 128 + ((chunk_lo ^ (ti & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(smem + kOffP + (g & 1) * kPBuf + ti * 128 + ((chunk_lo ^ (ti & 7)) << 4)) =
                 make_uint4(pl[4 * cc], pl[4 * cc + 1], pl[4 * cc + 2], pl[4 * cc + 3]);
           }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(ms.p_full));
+        mbar_arrive(bar(ms.p_full[g & 1]));
       }
       // Q of the next item while this item's last P.V runs
       if (it + 1 < item_end) q_prep(load_item(cp, ptr, it + 1), ii + 1);
@@ -742,12 +749,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             } else {
               // the first P.V of an item overwrites O^T: the previous epilogue must be done
               if (j == 0 && ii >= 1 && !(ok = mbar_wait(bar(ms.o_free), (ii - 1) & 1, abort_flag, ptr.err))) break;
-              if (!(ok = mbar_wait(bar(ms.p_full), g & 1, abort_flag, ptr.err))) break;
+              if (!(ok = mbar_wait(bar(ms.p_full[g & 1]), (g >> 1) & 1, abort_flag, ptr.err))) break;
               const uint32_t st = g % kVStages;
               if (!(ok = mbar_wait(bar(ms.v_full[st]), (g / kVStages) & 1, abort_flag, ptr.err))) break;
               tc_fence_after();
               const uint64_t a0 = smem_desc(sbase + kOffV + st * kKVTile, 1024, 1024, kSw128);
-              const uint64_t b0 = smem_desc(sbase + kOffP, 1024, 1024, kSw128);
+              const uint64_t b0 = smem_desc(sbase + kOffP + (g & 1) * kPBuf, 1024, 1024, kSw128);
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -758,7 +765,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                 }
               }
               mma_commit(bar(ms.v_empty[st]));
-              mma_commit(bar(ms.p_free));
+              mma_commit(bar(ms.pv_done[g & 1]));
               if (j == I.ntiles - 1) mma_commit(bar(ms.o_ready));
             }
           }
