@@ -62,6 +62,20 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(values, world: int, device) -> list:
+    """Each rank's timings -> the maximum over ranks (the slowest replica sets the job time)."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_value(units_per_step: float, world: int, step_ms: float) -> float:
+    """Replicas (weak scaling): every rank processes units_per_step per step, so the job's
+    throughput is world x units_per_step over the slowest rank's step time."""
+    return units_per_step * world / (step_ms / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -261,10 +275,7 @@ def run_ours(args, rank, world, local):
         e2e = (e2e_ms, h2d, d2h)
 
     # reduce over ranks: max time
-    t = torch.tensor([step_ms, kern_avg_ms, e2e[0] if e2e else 0.0], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    step_ms, kern_avg_ms, e2e_ms = t.tolist()
+    step_ms, kern_avg_ms, e2e_ms = max_over_ranks([step_ms, kern_avg_ms, e2e[0] if e2e else 0.0], world, dev)
     if rank != 0:
         return None
 
@@ -279,7 +290,7 @@ def run_ours(args, rank, world, local):
         kern_units = spec.flops / 1e12
         peak, peak_unit = 2 * bf16, "TFLOP/s"  # FP8 dense = 2 x measured bf16 (nominal ratio)
         traffic_kind = "prefill"
-    value = per_step * world / (step_ms / 1e3)
+    value = whole_job_value(per_step, world, step_ms)
     achieved = kern_units / (kern_avg_ms / 1e3)
     used = plan["path_bits"]
     kernel_kind = traffic_kind if used & (2 << dominant_cls) else "portable"
