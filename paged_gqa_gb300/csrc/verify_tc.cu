@@ -114,7 +114,7 @@ struct Misc {
   alignas(16) float merge_w[kMergeMaxSplits * kSlotRows];
   alignas(8) uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], s_free[2];
-  uint64_t p_full[kPBufs], pv_done[kPBufs], q_full, q_free, o_ready, o_free, drain[2];
+  uint64_t p_full[kPBufs], pv_done[kPBufs], q_full, q_free, o_ready, o_free, drain[2], merge_full;
   float qscale[2];
   float amax[kSoftWarps];
   uint32_t tmem_base;
@@ -212,6 +212,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     mbar_init(bar(ms.o_free), kSoftThreads);
     mbar_init(bar(ms.drain[0]), 1);
     mbar_init(bar(ms.drain[1]), 1);
+    mbar_init(bar(ms.merge_full), 1);
     ms.abort_flag = 0;
     fence_mbar_init();
   }
@@ -243,6 +244,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
     for (int n = 0; n < kCols; ++n) l[n] = 0.f;
     bool bad = false;
+    uint32_t merge_phase = 0;  // phases of merge_full used so far
 
     auto q_prep = [&](const Item& I, int ii) {
       const int pi = ii & 1;
@@ -611,14 +613,88 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           slot_lse(cp, slot)[row] = my_l > 0.f ? ms.m[pi][row] - kSigma + log2f(my_l) : -INFINITY;
         }
         __threadfence();
-        RowBlock rb;
-        rb.seq = I.seq;
-        rb.kvh = I.kvh;
-        rb.row0 = I.row0;
-        rb.nrows = I.nrows;
-        rb.nsplit = I.nsplit;
-        rb.slot_base = I.slot_base;
-        finish_split_block(p, ptr, cp, I.block, rb, gi, kSoftThreads, 2, &ms.merge_flag, ms.merge_w);
+        if (it + 1 == item_end && I.nsplit <= kMergeMaxSplits) {
+          // The CTA's last item: its K, V and P buffers are idle (every tile consumed, every
+          // MMA complete), so if this piece is the block's last, the merge bulk-loads the
+          // pieces' partials into them instead of reading them element by element (this
+          // merge is the tail of the kernel).
+          named_barrier(2, kSoftThreads);
+          if (gi == 0) {
+            __threadfence();
+            const int old = atomicAdd(&cp.counters[I.block], 1);
+            ms.merge_flag = old == I.nsplit - 1;
+            __threadfence();
+          }
+          named_barrier(2, kSoftThreads);
+          if (ms.merge_flag) {
+            __threadfence();
+            const int ns = I.nsplit;
+            constexpr uint32_t kRegion = kOffMisc - kOffK;  // K stages, V stages, P buffers
+            constexpr uint32_t kRowBytes = kHeadDim * 4;
+            const int rpp = min(kVN, (int)(kRegion / (ns * kRowBytes)) / 8 * 8);  // rows per pass
+            for (int r0 = 0; r0 < I.nrows; r0 += rpp) {
+              const int nr = min(rpp, I.nrows - r0);
+              if (gi == 0) {
+                fence_proxy_async_global();  // the partials are read by the async proxy
+                fence_proxy_async_smem();    // after the generic accesses to these buffers
+                mbar_expect_tx(bar(ms.merge_full), (uint32_t)(ns * nr) * kRowBytes);
+                for (int i = 0; i < ns; ++i)
+                  bulk_load(sbase + kOffK + (uint32_t)(i * rpp) * kRowBytes,
+                            slot_o(cp, I.slot_base + i) + (size_t)r0 * kHeadDim, (uint32_t)nr * kRowBytes,
+                            bar(ms.merge_full));
+              }
+              if (r0 == 0) {
+                // per-row weights 2^(lse_i - M) / sum while the partials load
+                for (int r = gi; r < I.nrows; r += kSoftThreads) {
+                  float lse[kMergeMaxSplits];
+                  float M = -INFINITY;
+#pragma unroll
+                  for (int i = 0; i < kMergeMaxSplits; ++i) {
+                    lse[i] = i < ns ? __ldcg(slot_lse(cp, I.slot_base + i) + r) : -INFINITY;
+                    M = fmaxf(M, lse[i]);
+                  }
+                  float sum = 0.f;
+#pragma unroll
+                  for (int i = 0; i < kMergeMaxSplits; ++i) {
+                    lse[i] = lse[i] == -INFINITY ? 0.f : exp2f(lse[i] - M);
+                    sum += lse[i];
+                  }
+                  const float inv_sum = sum > 0.f ? 1.f / sum : 0.f;
+#pragma unroll
+                  for (int i = 0; i < kMergeMaxSplits; ++i)
+                    if (i < ns) ms.merge_w[i * kSlotRows + r] = lse[i] * inv_sum;
+                }
+                named_barrier(2, kSoftThreads);
+              }
+              if (!mbar_wait(bar(ms.merge_full), merge_phase & 1, abort_flag, ptr.err)) bad = true;
+              ++merge_phase;
+              for (int idx = gi; idx < nr * (kHeadDim / 4); idx += kSoftThreads) {
+                const int r = idx / (kHeadDim / 4), d = (idx % (kHeadDim / 4)) * 4;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int i = 0; i < ns; ++i) {
+                  const float w = ms.merge_w[i * kSlotRows + r0 + r];
+                  const float4 o = *reinterpret_cast<const float4*>(smem + kOffK + (size_t)(i * rpp + r) * kRowBytes + d * 4);
+                  acc.x += w * o.x;
+                  acc.y += w * o.y;
+                  acc.z += w * o.z;
+                  acc.w += w * o.w;
+                }
+                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(ptr.out) + ms.out_off[pi][r0 + r] + d) =
+                    make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+              }
+              named_barrier(2, kSoftThreads);  // the buffers are reused by the next pass
+            }
+          }
+        } else {
+          RowBlock rb;
+          rb.seq = I.seq;
+          rb.kvh = I.kvh;
+          rb.row0 = I.row0;
+          rb.nrows = I.nrows;
+          rb.nsplit = I.nsplit;
+          rb.slot_base = I.slot_base;
+          finish_split_block(p, ptr, cp, I.block, rb, gi, kSoftThreads, 2, &ms.merge_flag, ms.merge_w);
+        }
       }
 #pragma unroll
       for (int n = 0; n < kCols; ++n) l[n] = 0.f;
