@@ -355,15 +355,17 @@ def _oracle_sample(spec, case, target_s, kind):
         elapsed += dt
         done_pairs += pairs_of(rows.tolist())
         rows_used += len(rows)
-        if elapsed >= target_s or n >= nrows_all:
+        if elapsed >= target_s:
             break
+        # grow the sample; once it covers the pool, keep timing fresh draws from it until the
+        # target time is reached (a small workload can take well under target_s in full)
         n = min(nrows_all, int(n * max(2.0, min(8.0, target_s / max(dt, 1e-3)))))
     est_total_s = elapsed * total_pairs / max(done_pairs, 1)
     if kind == "hbm":
         value, unit = spec.kv_bytes / 1e9 / est_total_s, "GB/s"
     else:
         value, unit = spec.flops / 1e12 / est_total_s, "TFLOP/s"
-    sample = (f"{rows_used} (token, head) rows drawn from {len(seq_ids)} random sequences of the workload; "
+    sample = (f"{rows_used} (token, head) row draws from {len(seq_ids)} random sequences of the workload; "
               f"{done_pairs} (row, key) pairs in {elapsed:.1f} s; scaled by the workload's {total_pairs} pairs")
     return {"value": value, "unit": unit, "cores": threads, "kind": "oracle", "sample": sample,
             "est_full_s": est_total_s, "sample_s": elapsed}
