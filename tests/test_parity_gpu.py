@@ -95,6 +95,33 @@ def test_plan_beyond_shared_memory_caches(path):
     gu.check_full(case, gu.run_library(case), "beyond plan caches")
 
 
+def test_decode_batch(path):
+    """Pure decode: every sequence has one new token (q_len 1), G = 8, two kv heads."""
+    gen = torch.Generator().manual_seed(31)
+    seqs = [(1, int(L)) for L in torch.randint(1, 3000, (40,), generator=gen)]
+    spec = wl.CaseSpec("decode", seqs, 16, 2, 16)
+    case = wl.make_case(spec, device="cuda", seed=31, poison=True)
+    gu.check_full(case, gu.run_library(case), "decode batch")
+
+
+def test_longer_mtp_q5_to_q8(path):
+    """q_len 5-8 with G = 16: 80-128 rows per kv head, past the 64-row verify blocks."""
+    gen = torch.Generator().manual_seed(32)
+    seqs = [(int(q), int(L)) for q, L in zip(torch.randint(5, 9, (24,), generator=gen),
+                                                torch.randint(8, 2500, (24,), generator=gen))]
+    spec = wl.CaseSpec("mtp q5-8", seqs, 16, 1, 16)
+    case = wl.make_case(spec, device="cuda", seed=32, poison=True)
+    gu.check_full(case, gu.run_library(case), "mtp q5-8")
+
+
+@pytest.mark.parametrize("q_dtype", ["bf16", "e4m3"])
+def test_group_of_32(path, q_dtype):
+    """G = 32 (32 q heads on one kv head): 32-128 rows for q_len 1-4, both block classes."""
+    spec = wl.CaseSpec("g32", [(1, 700), (2, 900), (3, 1300), (4, 400)], 32, 1, 64, q_dtype=q_dtype)
+    case = wl.make_case(spec, device="cuda", seed=33, poison=True)
+    gu.check_full(case, gu.run_library(case), f"G=32 {q_dtype}")
+
+
 def test_long_single_sequence_is_split(path):
     """One sequence, one kv head: its keys are cut across all CTAs and merged."""
     spec = wl.CaseSpec("long", [(4, 40000)], 16, 1, 16)
