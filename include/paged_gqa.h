@@ -144,6 +144,34 @@ int paged_gqa_attn_noalloc(const pg_tensor* q, const pg_tensor* k_cache, const p
                            float softmax_scale, pg_tensor* out, pg_stream_t stream);
 
 /*
+ * paged_gqa_cache_write -- the step before the call: write the new tokens' K and V into
+ * the paged FP8 cache it reads ("Optimize Qwen3.5 MTP unified attention on gfx950" and
+ * "asm FP8 FMHA for prefix-hit prefill" read such a cache; this fills it).
+ *
+ *   k_new, v_new    [T, Hkv, 256]       bf16, the new tokens in query_start_loc order;
+ *                                        head_dim contiguous, base and strides multiples
+ *                                        of 16 bytes
+ *   k_cache, v_cache [NB, P, Hkv, 256]  e4m3, written in place (same layout rules as the
+ *                                        call's caches)
+ *   block_table, seq_lens, query_start_loc  as in paged_gqa_attn: sequence s's q_len =
+ *                                        qsl[s+1] - qsl[s] new tokens take positions
+ *                                        seq_lens[s] - q_len .. seq_lens[s] - 1
+ *   k_descale, v_descale                the per-tensor descales the call multiplies back
+ *                                        (finite, > 0)
+ *
+ * Token t of sequence s lands in page block_table[s][pos / P], slot pos % P, as the e4m3
+ * codes of value / descale (computed in fp32, clamped to +-448, rounded to nearest even).
+ * Nothing else in the caches changes. Host-side argument errors return a status before any
+ * launch; a position or page id out of range is flagged in the device error word
+ * (PG_ERR_DEVICE_BOUNDS via paged_gqa_check_device_errors) and that row is skipped.
+ * Allocates nothing.
+ */
+int paged_gqa_cache_write(const pg_tensor* k_new, const pg_tensor* v_new, const pg_tensor* k_cache,
+                          const pg_tensor* v_cache, const pg_tensor* block_table, const pg_tensor* seq_lens,
+                          const pg_tensor* query_start_loc, float k_descale, float v_descale,
+                          pg_stream_t stream);
+
+/*
  * Workspace bytes for a call with these host-known sizes on `device`
  * (num_seqs, total query tokens T, heads, page size, block-table width W).
  * Returns 0 on invalid sizes.

@@ -15,7 +15,8 @@ STATUS_NAMES = {0: "PG_OK", -1: "PG_ERR_INVALID_ARG", -2: "PG_ERR_UNSUPPORTED", 
                 -4: "PG_ERR_TIMEOUT", -5: "PG_ERR_DEVICE_BOUNDS", -6: "PG_ERR_WORKSPACE"}
 
 # Every symbol include/paged_gqa.h declares.
-EXPORTED = ("paged_gqa_attn", "paged_gqa_attn_ex", "paged_gqa_attn_noalloc", "paged_gqa_workspace_size",
+EXPORTED = ("paged_gqa_attn", "paged_gqa_attn_ex", "paged_gqa_attn_noalloc", "paged_gqa_cache_write",
+            "paged_gqa_workspace_size",
             "paged_gqa_last_error",
             "paged_gqa_check_device_errors", "paged_gqa_set_path", "paged_gqa_last_plan",
             "paged_gqa_set_kernel_events", "paged_gqa_version")
@@ -56,6 +57,8 @@ def load(build_if_missing: bool = True):
             lib.paged_gqa_attn.restype = ctypes.c_int
             lib.paged_gqa_attn_ex.argtypes = [P, P, P, P, P, P, f, f, f, f, P, c_vp, ctypes.c_size_t, c_vp]
             lib.paged_gqa_attn_ex.restype = ctypes.c_int
+            lib.paged_gqa_cache_write.argtypes = [P, P, P, P, P, P, P, f, f, c_vp]
+            lib.paged_gqa_cache_write.restype = ctypes.c_int
             lib.paged_gqa_workspace_size.argtypes = [ctypes.c_int] * 7
             lib.paged_gqa_workspace_size.restype = ctypes.c_size_t
             lib.paged_gqa_last_error.restype = ctypes.c_char_p
@@ -137,6 +140,16 @@ def paged_gqa_attn_ex(q, k_cache, v_cache, block_table, seq_lens, query_start_lo
     _check(lib.paged_gqa_attn_ex(*[ctypes.byref(x) for x in a], float(q_descale), float(k_descale),
                                  float(v_descale), float(softmax_scale), ctypes.byref(o), ptr, nbytes,
                                  _stream(stream)))
+
+
+def paged_gqa_cache_write(k_new, v_new, k_cache, v_cache, block_table, seq_lens, query_start_loc,
+                          k_descale: float, v_descale: float, stream=None) -> None:
+    """Write the new tokens' K and V (bf16 [T, Hkv, 256]) into the e4m3 paged caches."""
+    lib = load()
+    a = [_desc(k_new), _desc(v_new), _desc(k_cache), _desc(v_cache), _desc(block_table), _desc(seq_lens),
+         _desc(query_start_loc)]
+    _check(lib.paged_gqa_cache_write(*[ctypes.byref(x) for x in a], float(k_descale), float(v_descale),
+                                     _stream(stream)))
 
 
 def paged_gqa_workspace_size(num_seqs: int, total_q: int, num_q_heads: int, num_kv_heads: int,

@@ -438,6 +438,93 @@ int paged_gqa_set_kernel_events(int cls, void* start, void* stop) {
   return PG_OK;
 }
 
+int paged_gqa_cache_write(const pg_tensor* k_new, const pg_tensor* v_new, const pg_tensor* k_cache,
+                          const pg_tensor* v_cache, const pg_tensor* block_table, const pg_tensor* seq_lens,
+                          const pg_tensor* query_start_loc, float k_descale, float v_descale, pg_stream_t stream) {
+  int st;
+  if ((st = check_tensor(k_new, "k_new", 3)) || (st = check_tensor(v_new, "v_new", 3)) ||
+      (st = check_tensor(k_cache, "k_cache", 4)) || (st = check_tensor(v_cache, "v_cache", 4)) ||
+      (st = check_tensor(block_table, "block_table", 2)) || (st = check_tensor(seq_lens, "seq_lens", 1)) ||
+      (st = check_tensor(query_start_loc, "query_start_loc", 1)))
+    return st;
+  if (k_new->dtype != PG_BF16 || v_new->dtype != PG_BF16)
+    return fail(PG_ERR_UNSUPPORTED, "k_new and v_new must be bf16");
+  if (k_cache->dtype != PG_E4M3 || v_cache->dtype != PG_E4M3)
+    return fail(PG_ERR_UNSUPPORTED, "the caches must be e4m3");
+  for (int i = 0; i < 3; ++i)
+    if (k_new->shape[i] != v_new->shape[i]) return fail(PG_ERR_INVALID_ARG, "k_new and v_new shapes differ");
+  for (int i = 0; i < 4; ++i)
+    if (k_cache->shape[i] != v_cache->shape[i]) return fail(PG_ERR_INVALID_ARG, "k_cache and v_cache shapes differ");
+  const long long T = k_new->shape[0], Hkv = k_new->shape[1];
+  const long long NB = k_cache->shape[0], P = k_cache->shape[1], S = seq_lens->shape[0], W = block_table->shape[1];
+  if (k_new->shape[2] != kHeadDim || k_cache->shape[3] != kHeadDim)
+    return fail(PG_ERR_UNSUPPORTED, "head_dim must be 256");
+  if (k_cache->shape[2] != Hkv) return fail(PG_ERR_INVALID_ARG, "k_new and the caches disagree on num_kv_heads");
+  if (P != 16 && P != 32 && P != 64 && P != 128)
+    return fail(PG_ERR_UNSUPPORTED, "page size %lld not in {16, 32, 64, 128}", P);
+  if (block_table->shape[0] != S || query_start_loc->shape[0] != S + 1)
+    return fail(PG_ERR_INVALID_ARG, "block_table rows / query_start_loc length must match seq_lens");
+  if (S == 0 && T > 0) return fail(PG_ERR_INVALID_ARG, "tokens without sequences");
+  if (T > INT32_MAX / 2 || NB > INT32_MAX || S > INT32_MAX / 2 || W > INT32_MAX / 2 || Hkv > 65535)
+    return fail(PG_ERR_UNSUPPORTED, "sizes beyond the supported range");
+  if (block_table->dtype != PG_I32 || seq_lens->dtype != PG_I32 || query_start_loc->dtype != PG_I32)
+    return fail(PG_ERR_INVALID_ARG, "block_table, seq_lens and query_start_loc must be int32");
+  if (k_new->stride[2] != 1 || v_new->stride[2] != 1 || k_cache->stride[3] != 1 || v_cache->stride[3] != 1)
+    return fail(PG_ERR_INVALID_ARG, "the head_dim axis must be contiguous");
+  if (W > 1 && block_table->stride[1] != 1) return fail(PG_ERR_INVALID_ARG, "block_table rows must be contiguous");
+  if ((S > 0 && seq_lens->stride[0] != 1) || query_start_loc->stride[0] != 1)
+    return fail(PG_ERR_INVALID_ARG, "seq_lens and query_start_loc must be contiguous");
+  if (!aligned16(k_new->data) || !aligned16(v_new->data) || !aligned16(k_cache->data) || !aligned16(v_cache->data))
+    return fail(PG_ERR_INVALID_ARG, "k_new, v_new and the caches must be 16-byte aligned");
+  for (int i = 0; i < 2; ++i)
+    if ((k_new->stride[i] * 2) % 16 || (v_new->stride[i] * 2) % 16)
+      return fail(PG_ERR_INVALID_ARG, "k_new/v_new strides must be multiples of 16 bytes");
+  for (int i = 0; i < 3; ++i)
+    if (k_cache->stride[i] % 16 || v_cache->stride[i] % 16)
+      return fail(PG_ERR_INVALID_ARG, "cache strides must be multiples of 16 bytes");
+  if ((T > 0 && (!k_new->data || !v_new->data)) || (NB > 0 && (!k_cache->data || !v_cache->data)) ||
+      !query_start_loc->data || (S > 0 && (!seq_lens->data || (W > 0 && !block_table->data))))
+    return fail(PG_ERR_INVALID_ARG, "null data pointer");
+  if (!(std::isfinite(k_descale) && k_descale > 0.f && std::isfinite(v_descale) && v_descale > 0.f))
+    return fail(PG_ERR_INVALID_ARG, "descales must be finite and positive");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceState* ds = nullptr;
+  if ((st = device_state(dev, &ds)) != PG_OK) return st;
+  CacheWriteArgs a;
+  a.kn = static_cast<const uint16_t*>(k_new->data);
+  a.vn = static_cast<const uint16_t*>(v_new->data);
+  a.kn_st = k_new->stride[0];
+  a.kn_sh = k_new->stride[1];
+  a.vn_st = v_new->stride[0];
+  a.vn_sh = v_new->stride[1];
+  a.kc = static_cast<uint8_t*>(k_cache->data);
+  a.vc = static_cast<uint8_t*>(v_cache->data);
+  a.kc_sb = k_cache->stride[0];
+  a.kc_sp = k_cache->stride[1];
+  a.kc_sh = k_cache->stride[2];
+  a.vc_sb = v_cache->stride[0];
+  a.vc_sp = v_cache->stride[1];
+  a.vc_sh = v_cache->stride[2];
+  a.bt = static_cast<const int32_t*>(block_table->data);
+  a.bt_stride = W > 0 ? block_table->stride[0] : 1;
+  a.seq_lens = static_cast<const int32_t*>(seq_lens->data);
+  a.qsl = static_cast<const int32_t*>(query_start_loc->data);
+  a.num_seqs = (int)S;
+  a.T = (int)T;
+  a.Hkv = (int)Hkv;
+  a.P = (int)P;
+  a.W = (int)W;
+  a.NB = (int)NB;
+  a.k_scale = 1.f / k_descale;
+  a.v_scale = 1.f / v_descale;
+  a.err = ds->err;
+  e = launch_cache_write(a, ds->sms, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cache write launch");
+  return PG_OK;
+}
+
 int paged_gqa_version(void) { return 100; }
 
 }  // extern "C"

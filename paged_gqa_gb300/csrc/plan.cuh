@@ -7,6 +7,25 @@ namespace pgqa {
 cudaError_t launch_plan(const Problem& p, const Pointers& ptr, const ClassPlan& verify,
                         const ClassPlan& prefill, cudaStream_t stream);
 
+// Arguments of the paged KV-cache write (cache_write.cu); strides in elements.
+struct CacheWriteArgs {
+  const uint16_t* kn;
+  const uint16_t* vn;
+  long long kn_st, kn_sh, vn_st, vn_sh;  // elements
+  uint8_t* kc;
+  uint8_t* vc;
+  long long kc_sb, kc_sp, kc_sh, vc_sb, vc_sp, vc_sh;  // bytes (elements of 1 byte)
+  const int32_t* bt;
+  long long bt_stride;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  int num_seqs, T, Hkv, P, W, NB;
+  float k_scale, v_scale;  // 1 / descale
+  uint32_t* err;
+};
+// Paged KV-cache write (cache_write.cu): new tokens' K and V -> e4m3 codes in their pages.
+cudaError_t launch_cache_write(const CacheWriteArgs& a, int sms, cudaStream_t stream);
+
 // Warp-level MMA (mma.sync, tf32) kernel for one class's items; any dtype mix.
 cudaError_t launch_portable(const Problem& p, const Pointers& ptr, const ClassPlan& cp,
                             int block_rows, cudaStream_t stream);

@@ -121,3 +121,40 @@ def test_set_path_roundtrip():
     assert pg.paged_gqa_set_path(prev) == 1
     with pytest.raises(pg.PagedGQAError):
         pg.paged_gqa_set_path(7)
+
+
+def _cw_args(**over):
+    a = dict(
+        kn=FakeTensor((8, 2, 256), torch.bfloat16),
+        vn=FakeTensor((8, 2, 256), torch.bfloat16),
+        kc=FakeTensor((10, 16, 2, 256), torch.uint8),
+        vc=FakeTensor((10, 16, 2, 256), torch.uint8),
+        bt=FakeTensor((2, 5), torch.int32),
+        sl=FakeTensor((2,), torch.int32),
+        qsl=FakeTensor((3,), torch.int32),
+    )
+    a.update(over)
+    return a
+
+
+def _cw_call(a, kd=1.0, vd=1.0):
+    d = [B._desc(a[n]) for n in ("kn", "vn", "kc", "vc", "bt", "sl", "qsl")]
+    return pg.load().paged_gqa_cache_write(*[ctypes.byref(x) for x in d], kd, vd, None)
+
+
+@pytest.mark.parametrize("over,scales,code,msg", [
+    (dict(kn=FakeTensor((8, 2, 256), torch.uint8)), (1.0, 1.0), -2, "bf16"),
+    (dict(kc=FakeTensor((10, 16, 2, 256), torch.bfloat16), vc=FakeTensor((10, 16, 2, 256), torch.bfloat16)),
+     (1.0, 1.0), -2, "e4m3"),
+    (dict(kc=FakeTensor((10, 16, 4, 256), torch.uint8), vc=FakeTensor((10, 16, 4, 256), torch.uint8)),
+     (1.0, 1.0), -1, "num_kv_heads"),
+    (dict(kn=FakeTensor((8, 2, 128), torch.bfloat16), vn=FakeTensor((8, 2, 128), torch.bfloat16)), (1.0, 1.0), -2,
+     "head_dim"),
+    (dict(kn=FakeTensor((8, 2, 256), torch.bfloat16, stride=[516, 258, 1])), (1.0, 1.0), -1, "16 bytes"),
+    (dict(qsl=FakeTensor((2,), torch.int32)), (1.0, 1.0), -1, "query_start_loc"),
+    ({}, (0.0, 1.0), -1, "positive"),
+    ({}, (1.0, float("nan")), -1, "positive"),
+])
+def test_cache_write_rejects_bad_arguments_before_any_launch(over, scales, code, msg):
+    assert _cw_call(_cw_args(**over), *scales) == code
+    assert msg in B.paged_gqa_last_error()
