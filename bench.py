@@ -6,6 +6,7 @@ FP8 e4m3 K/V with per-tensor descales, bf16 Q and output. One step = one
 paged_gqa_attn call (plan + attention kernels) over that batch.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl reference]
+  python bench.py --op cache_write [--config 1..5] ...   # the paged KV-cache write alone
 
 Prints ONE JSON line (rank 0). The value is KV-read GB/s (algorithmic bytes: each
 valid token's K and V once per kv head) for verify-bound workloads and TFLOP/s
@@ -16,10 +17,19 @@ slowest rank's time.
 
 --impl reference times the fp64 CPU oracle (the only reference this path has) on a
 bounded sample of the same workload on the host cores.
+
+--op attn_quant_q times paged_gqa_attn_quant_q: the same workload with its bf16 Q
+quantised inside the call to e4m3 under one per-tensor scale (amax / 448).
+
+--op cache_write times paged_gqa_cache_write instead: the config's new tokens (every
+sequence's last q_len positions, bf16 K and V for each kv head) quantised to e4m3 and
+scattered into their pages. Its value is GB/s of algorithmic bytes (per (token, kv head)
+row: 2 x 512 bytes of bf16 read, 2 x 256 bytes of e4m3 written) against the HBM roofline.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import hashlib
 import os
@@ -49,6 +59,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--op", default="attn", choices=["attn", "attn_quant_q", "cache_write"])
+    ap.add_argument("--write-case", default="config", choices=["config", "chunks"],
+                    help="cache_write: the config's new tokens, or 32 fresh 4096-token chunks (profiling size)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -95,8 +108,8 @@ def workload_kind(spec: wl.CaseSpec) -> str:
     return "hbm" if t_mem >= t_mma else "tensor"
 
 
-def config_dict(spec: wl.CaseSpec, idx: int, n: int, l2_note: str):
-    return {"workload": spec.name, "config_index": idx, "num_seqs": spec.num_seqs, "total_q": spec.total_q,
+def config_dict(spec: wl.CaseSpec, idx: int, n: int, l2_note: str, quant_q: bool = False):
+    return {"workload": spec.name + (":quant_q" if quant_q else ""), "config_index": idx, "num_seqs": spec.num_seqs, "total_q": spec.total_q,
             "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads, "head_dim": wl.HEAD_DIM,
             "page_size": spec.page_size, "q_dtype": spec.q_dtype, "kv_dtype": spec.kv_dtype, "out_dtype": "bf16",
             "kv_bytes": spec.kv_bytes, "flops": spec.flops, "parallelism": f"replicas{n}", "l2": l2_note,
@@ -162,7 +175,8 @@ class ClockSampler:
 
 
 def kernel_source_hash(cls_kind: str) -> str:
-    names = {"verify": ["verify_tc.cu"], "prefill": ["prefill_tc.cu"], "portable": ["portable.cu"]}[cls_kind]
+    names = {"verify": ["verify_tc.cu"], "prefill": ["prefill_tc.cu"], "portable": ["portable.cu"],
+             "cache_write": ["cache_write.cu"]}[cls_kind]
     h = hashlib.sha256()
     for n in names + ["common.cuh", "device_util.cuh", "tc_util.cuh"]:
         p = os.path.join(ROOT, "paged_gqa_gb300", "csrc", n)
@@ -202,9 +216,14 @@ def run_ours(args, rank, world, local):
     if args.config == 5:
         dominant_cls = 1
 
+    quant_q = args.op == "attn_quant_q"
+    if quant_q and spec.q_dtype != "bf16":
+        raise SystemExit(f"--op attn_quant_q needs a workload with a bf16 q (config {args.config} has {spec.q_dtype})")
+    attn = pg.paged_gqa_attn_quant_q if quant_q else pg.paged_gqa_attn
+
     def call():
-        pg.paged_gqa_attn(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
-                          case.query_start_loc, case.k_descale, case.v_descale, case.softmax_scale, out)
+        attn(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+             case.query_start_loc, case.k_descale, case.v_descale, case.softmax_scale, out)
 
     for _ in range(max(3, args.warmup)):
         call()
@@ -257,8 +276,8 @@ def run_ours(args, rank, world, local):
         def e2e_step():
             for h, d in zip(host_in, dev_in):
                 d.copy_(h, non_blocking=True)
-            pg.paged_gqa_attn(dev_in[0], case.k_cache, case.v_cache, dev_in[1], dev_in[2], dev_in[3],
-                              case.k_descale, case.v_descale, case.softmax_scale, out)
+            attn(dev_in[0], case.k_cache, case.v_cache, dev_in[1], dev_in[2], dev_in[3],
+                 case.k_descale, case.v_descale, case.softmax_scale, out)
             host_out.copy_(out, non_blocking=True)
 
         for _ in range(3):
@@ -299,7 +318,7 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "us_per_call": round(step_ms * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if kernel_kind != "portable" else "tf32",
         "data": "synthetic (seeded N(0,1), FP8 per-tensor amax/448)",
-        "config": config_dict(spec, args.config, world, "flushed: 512 MiB memset between timed calls"),
+        "config": config_dict(spec, args.config, world, "flushed: 512 MiB memset between timed calls", quant_q),
         "roofline": {"bound": kind, "achieved": round(achieved, 2), "peak": peak, "unit": peak_unit,
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} ({'hbm_gbs' if kind == 'hbm' else '2 x bf16_tflops burst'})",
                      "kernel": kernel_kind, "kernel_us": round(kern_avg_ms * 1e3, 2),
@@ -313,16 +332,206 @@ def run_ours(args, rank, world, local):
                       "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2],
                       "note": "per step: q, block_table, seq_lens, query_start_loc H2D from pinned memory; out D2H; KV cache resident"}
     if world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(spec, case, args.cpu_seconds, kind)
+        res["cpu_baseline"] = cpu_baseline(spec, case, args.cpu_seconds, kind, quant_q)
     return res
+
+
+# ----------------------------------------------------------- cache write --
+
+CW_ROW_BYTES = 2 * wl.HEAD_DIM * 2 + 2 * wl.HEAD_DIM  # bf16 K and V read, e4m3 K and V written
+CW_METRIC = "GB/s of the paged KV-cache write (bf16 new K/V read + e4m3 pages written) as % of HBM roofline"
+
+
+def cw_config(spec: wl.CaseSpec, idx: int, n: int, l2_note: str):
+    rows = spec.total_q * spec.num_kv_heads
+    return {"workload": "cache_write:" + spec.name, "config_index": idx, "num_seqs": spec.num_seqs,
+            "new_tokens": spec.total_q, "num_kv_heads": spec.num_kv_heads, "head_dim": wl.HEAD_DIM,
+            "page_size": spec.page_size, "in_dtype": "bf16", "cache_dtype": "e4m3", "rows": rows,
+            "bytes": rows * CW_ROW_BYTES, "parallelism": f"replicas{n}", "l2": l2_note, "seed": 0}
+
+
+def _cw_spec(args) -> wl.CaseSpec:
+    if args.write_case == "chunks":
+        return wl.write_chunks_spec()
+    return dataclasses.replace(wl.config_spec(args.config), kv_dtype="e4m3")
+
+
+def _new_tokens(spec, device, seed):
+    g = torch.Generator(device=device).manual_seed(seed + 101)
+    shape = (spec.total_q, spec.num_kv_heads, wl.HEAD_DIM)
+    kn = torch.randn(shape, generator=g, device=device).to(torch.bfloat16)
+    vn = torch.randn(shape, generator=g, device=device).to(torch.bfloat16)
+    return kn, vn
+
+
+def run_cache_write(args, rank, world, local):
+    import paged_gqa_gb300 as pg
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg.load()
+    spec = _cw_spec(args)
+    case = wl.make_case(spec, device=dev, seed=rank)
+    kn, vn = _new_tokens(spec, dev, rank)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    bytes_per_step = spec.total_q * spec.num_kv_heads * CW_ROW_BYTES
+
+    def call(k_new=kn, v_new=vn, bt=case.block_table, sl=case.seq_lens, qsl=case.query_start_loc):
+        pg.paged_gqa_cache_write(k_new, v_new, case.k_cache, case.v_cache, bt, sl, qsl,
+                                 case.k_descale, case.v_descale)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    assert pg.paged_gqa_check_device_errors() == 0, pg.paged_gqa_last_error()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()  # L2 flush between timed iterations (outside the events)
+        ev[i][0].record()
+        call()  # one kernel per call: the events bracket that kernel alone
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+
+    e2e = None
+    if not args.no_e2e:
+        src = (kn, vn, case.block_table, case.seq_lens, case.query_start_loc)
+        host_in = [t.cpu().pin_memory() for t in src]
+        dev_in = [torch.empty_like(t) for t in src]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+
+        def e2e_step():
+            for h, d in zip(host_in, dev_in):
+                d.copy_(h, non_blocking=True)
+            call(*dev_in)
+            # the step's result on the host: the device status word (synchronises the stream)
+            assert pg.paged_gqa_check_device_errors() == 0
+
+        for _ in range(3):
+            e2e_step()
+        e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            flush.zero_()
+            e_ev[i][0].record()
+            e2e_step()
+            e_ev[i][1].record()
+        torch.cuda.synchronize()
+        e2e = (sum(a.elapsed_time(b) for a, b in e_ev) / K, h2d, 4)
+
+    step_ms, e2e_ms = max_over_ranks([step_ms, e2e[0] if e2e else 0.0], world, dev)
+    if rank != 0:
+        return None
+    hbm, _, _, peak_src = load_peaks()
+    value = whole_job_value(bytes_per_step / 1e9, world, step_ms)
+    achieved = bytes_per_step / 1e9 / (step_ms / 1e3)
+    res = {
+        "metric": CW_METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "us_per_call": round(step_ms * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3",
+        "data": "synthetic (seeded N(0,1) new K/V; the config's paged cache and block table)",
+        "config": cw_config(spec, args.config, world, "flushed: 512 MiB memset between timed calls"),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "peak_source": f"{peak_src} (hbm_gbs)",
+                     "kernel": "cache_write", "kernel_us": round(step_ms * 1e3, 2),
+                     "traffic": cw_traffic(spec)},
+        "gpu_launches": K, "clocks": clocks, "wall_s": round(wall, 3),
+    }
+    if e2e:
+        res["e2e"] = {"value": round(bytes_per_step * world / 1e9 / (e2e_ms / 1e3), 3), "unit": "GB/s",
+                      "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2],
+                      "note": "per step: new K/V, block_table, seq_lens, query_start_loc H2D from pinned memory; "
+                              "the device status word D2H; the cache stays resident"}
+    if world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cw_cpu_sample(spec, case, kn, vn, args.cpu_seconds)
+    return res
+
+
+def cw_traffic(spec):
+    """DRAM bytes per launch: the committed capture's bytes per (token, kv head) row times
+    this workload's rows (the write's traffic grows with its rows), if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            e = json.load(f).get("cache_write:per_row")
+        if e and e.get("source_sha") == kernel_source_hash("cache_write"):
+            return round(float(e["dram_bytes_per_row"]) * spec.total_q * spec.num_kv_heads)
+    except Exception:
+        pass
+    return None
+
+
+def cw_cpu_sample(spec, case, kn, vn, target_s):
+    """The write oracle on random whole sequences until ~target_s; scaled to the workload's rows."""
+    from oracle import cache_write as cw
+    gen = torch.Generator().manual_seed(4321)
+    qsl = case.query_start_loc.cpu().tolist()
+    order = torch.randperm(spec.num_seqs, generator=gen).tolist()
+    elapsed, rows, nseq = 0.0, 0, 0
+    for s in order:
+        sub = wl.subcase(case, [s])
+        k_new = kn[qsl[s]:qsl[s + 1]].float().cpu().numpy()
+        v_new = vn[qsl[s]:qsl[s + 1]].float().cpu().numpy()
+        args = (sub.k_cache.numpy(), sub.v_cache.numpy(), sub.block_table.numpy(), sub.seq_lens.numpy(),
+                sub.query_start_loc.numpy(), case.k_descale, case.v_descale)
+        t0 = time.perf_counter()
+        cw.cache_write(k_new, v_new, *args)
+        elapsed += time.perf_counter() - t0
+        rows += k_new.shape[0] * k_new.shape[1]
+        nseq += 1
+        if elapsed >= target_s:
+            break
+    total_rows = spec.total_q * spec.num_kv_heads
+    est_s = elapsed * total_rows / max(rows, 1)
+    value = total_rows * CW_ROW_BYTES / 1e9 / est_s
+    return {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{nseq} random whole sequences ({rows} (token, kv head) rows) in {elapsed:.1f} s; "
+                      f"scaled by the workload's {total_rows} rows",
+            "est_full_s": round(est_s, 6), "sample_s": round(elapsed, 6)}
+
+
+def run_cache_write_reference(args, rank, world):
+    if rank != 0:
+        return None
+    spec = _cw_spec(args)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    case = wl.make_case(spec, device=dev, seed=0)
+    kn, vn = _new_tokens(spec, dev, 0)
+    per = max(1.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cw_cpu_sample(spec, case, kn, vn, per / 4)
+    runs = [cw_cpu_sample(spec, case, kn, vn, per) for _ in range(args.steps)]
+    value = statistics.median(r["value"] for r in runs)
+    est_s = statistics.median(r["est_full_s"] for r in runs)
+    return {"impl": "reference", "metric": CW_METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(est_s * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32->e4m3",
+            "data": "synthetic (seeded N(0,1) new K/V; the config's paged cache and block table)",
+            "config": cw_config(spec, args.config, world, "n/a (CPU)"),
+            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": runs[-1]["sample"]},
+            "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 # ------------------------------------------------------------------- oracle --
 
-def _oracle_sample(spec, case, target_s, kind):
-    """Time the oracle on growing row samples until ~target_s; scale to the workload."""
+def _oracle_sample(spec, case, target_s, kind, quant_q=False):
+    """Time the oracle on growing row samples until ~target_s; scale to the workload.
+
+    quant_q: the oracle of the quantising call (the whole Q's scale, timed once, then the
+    sampled rows' attention on their e4m3 codes)."""
     import numpy as np
     import oracle
+    from oracle import quant_q as qq
     threads = oracle.max_threads()
     gen = torch.Generator().manual_seed(1234)
     total_pairs = spec.flops // (4 * wl.HEAD_DIM)  # (row, visible key) pairs of the whole workload
@@ -347,10 +556,21 @@ def _oracle_sample(spec, case, target_s, kind):
     n = 8
     elapsed, done_pairs = 0.0, 0
     rows_used = 0
+    scales = None
+    if quant_q:
+        t0 = time.perf_counter()
+        scales = qq.q_scales(case.q.float().cpu().numpy())
+        elapsed += time.perf_counter() - t0
     while True:
         rows = torch.randperm(nrows_all, generator=gen)[: min(n, nrows_all)].sort().values.numpy().astype(np.int64)
         t0 = time.perf_counter()
-        oracle.attention_case(sub, rows=rows, threads=threads)
+        if quant_q:
+            qq.attention_quant_q(sub.q, sub.k_cache, sub.v_cache, sub.block_table, sub.seq_lens,
+                                 sub.query_start_loc, kv_dtype=spec.kv_dtype, k_descale=case.k_descale,
+                                 v_descale=case.v_descale, softmax_scale=spec.softmax_scale, rows=rows,
+                                 threads=threads, scales=scales)
+        else:
+            oracle.attention_case(sub, rows=rows, threads=threads)
         dt = time.perf_counter() - t0
         elapsed += dt
         done_pairs += pairs_of(rows.tolist())
@@ -371,8 +591,8 @@ def _oracle_sample(spec, case, target_s, kind):
             "est_full_s": est_total_s, "sample_s": elapsed}
 
 
-def cpu_baseline(spec, case, target_s, kind):
-    r = _oracle_sample(spec, case, target_s, kind)
+def cpu_baseline(spec, case, target_s, kind, quant_q=False):
+    r = _oracle_sample(spec, case, target_s, kind, quant_q)
     return {k: (round(v, 6) if isinstance(v, float) else v) for k, v in r.items()}
 
 
@@ -385,11 +605,12 @@ def run_reference(args, rank, world):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     case = wl.make_case(spec, device=dev, seed=0)
     per = max(1.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
+    quant_q = args.op == "attn_quant_q"
     for _ in range(args.warmup):
-        _oracle_sample(spec, case, per / 4, kind)
+        _oracle_sample(spec, case, per / 4, kind, quant_q)
     times, vals, last = [], [], None
     for _ in range(args.steps):
-        last = _oracle_sample(spec, case, per, kind)
+        last = _oracle_sample(spec, case, per, kind, quant_q)
         times.append(last["est_full_s"])
         vals.append(last["value"])
     est_s = statistics.median(times)
@@ -398,7 +619,7 @@ def run_reference(args, rank, world):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(est_s * 1e3, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": "f64", "data": "synthetic (seeded N(0,1), FP8 per-tensor amax/448)",
-           "config": config_dict(spec, args.config, world, "n/a (CPU)"),
+           "config": config_dict(spec, args.config, world, "n/a (CPU)", quant_q),
            "cpu_baseline": {"value": round(value, 6), "unit": last["unit"], "cores": last["cores"], "kind": "oracle",
                             "sample": last["sample"]},
            "e2e": {"value": round(value, 6), "unit": last["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -411,9 +632,9 @@ def main():
     if world > 1 and args.impl == "ours":
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     if args.impl == "reference":
-        res = run_reference(args, rank, world)
+        res = (run_cache_write_reference if args.op == "cache_write" else run_reference)(args, rank, world)
     else:
-        res = run_ours(args, rank, world, local)
+        res = (run_cache_write if args.op == "cache_write" else run_ours)(args, rank, world, local)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1 and args.impl == "ours":

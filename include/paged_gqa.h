@@ -144,6 +144,29 @@ int paged_gqa_attn_noalloc(const pg_tensor* q, const pg_tensor* k_cache, const p
                            float softmax_scale, pg_tensor* out, pg_stream_t stream);
 
 /*
+ * paged_gqa_attn_quant_q -- paged_gqa_attn on a bf16 q that the call first quantises to
+ * FP8 e4m3 with one per-tensor scale, so that Q . K^T runs as a single FP8 product
+ * ("asm FP8 FMHA for prefix-hit prefill": the FP8 prefill attention takes an e4m3 Q with a
+ * per-tensor scale, and its summary counts the Q cast inside the attention time).
+ *
+ * What it computes: amax = max |q| over the whole tensor (NaNs skipped); q_descale =
+ * amax / 448 and inv = 1 / q_descale, each rounded to nearest in fp32 (both 1 when amax
+ * is 0 or infinite); every element becomes the e4m3 code of q * inv (fp32 product, round
+ * to nearest even, saturating at +-448); then exactly paged_gqa_attn with that e4m3 q and
+ * q_descale. The e4m3 q is never written to memory: the attention kernels cast each Q
+ * tile as they stage it, after one extra launch that reads q to find amax.
+ *
+ * Arguments are those of paged_gqa_attn, except: q must be bf16 and the caches e4m3
+ * (else PG_ERR_UNSUPPORTED), and the tcgen05 path must be selected (paged_gqa_set_path
+ * 0, the default; else PG_ERR_UNSUPPORTED). Uses the library-owned workspace like
+ * paged_gqa_attn. Error behaviour as paged_gqa_attn.
+ */
+int paged_gqa_attn_quant_q(const pg_tensor* q, const pg_tensor* k_cache, const pg_tensor* v_cache,
+                           const pg_tensor* block_table, const pg_tensor* seq_lens,
+                           const pg_tensor* query_start_loc, float k_descale, float v_descale,
+                           float softmax_scale, pg_tensor* out, pg_stream_t stream);
+
+/*
  * paged_gqa_cache_write -- the step before the call: write the new tokens' K and V into
  * the paged FP8 cache it reads ("Optimize Qwen3.5 MTP unified attention on gfx950" and
  * "asm FP8 FMHA for prefix-hit prefill" read such a cache; this fills it).

@@ -52,10 +52,16 @@ def quantize_q(q: np.ndarray):
 
 
 def attention_quant_q(q_bf16, k_cache, v_cache, block_table, seq_lens, query_start_loc, *, kv_dtype: str,
-                      k_descale: float, v_descale: float, softmax_scale: float, rows=None, threads: int = 0):
-    """fp64 attention with Q quantised per tensor; q_bf16 is a torch bf16 tensor [T, Hq, 256]."""
+                      k_descale: float, v_descale: float, softmax_scale: float, rows=None, threads: int = 0,
+                      scales=None):
+    """fp64 attention with Q quantised per tensor; q_bf16 is a torch bf16 tensor [T, Hq, 256].
+
+    ``scales``: the (q_descale, inv) pair of the whole Q when q_bf16 holds only some of its
+    sequences (q_scales of the full tensor); by default they come from q_bf16 itself."""
     import torch
-    codes, d = quantize_q(q_bf16.detach().float().cpu().numpy())
+    q = q_bf16.detach().float().cpu().numpy()
+    d, inv = scales if scales is not None else q_scales(q)
+    codes = e4m3_encode((q * np.float32(inv)).astype(np.float32))
     q8 = torch.from_numpy(codes)
     return attention(q8, k_cache, v_cache, block_table, seq_lens, query_start_loc, q_dtype="e4m3",
                      kv_dtype=kv_dtype, q_descale=float(d), k_descale=k_descale, v_descale=v_descale,

@@ -15,7 +15,8 @@ STATUS_NAMES = {0: "PG_OK", -1: "PG_ERR_INVALID_ARG", -2: "PG_ERR_UNSUPPORTED", 
                 -4: "PG_ERR_TIMEOUT", -5: "PG_ERR_DEVICE_BOUNDS", -6: "PG_ERR_WORKSPACE"}
 
 # Every symbol include/paged_gqa.h declares.
-EXPORTED = ("paged_gqa_attn", "paged_gqa_attn_ex", "paged_gqa_attn_noalloc", "paged_gqa_cache_write",
+EXPORTED = ("paged_gqa_attn", "paged_gqa_attn_ex", "paged_gqa_attn_noalloc", "paged_gqa_attn_quant_q",
+            "paged_gqa_cache_write",
             "paged_gqa_workspace_size",
             "paged_gqa_last_error",
             "paged_gqa_check_device_errors", "paged_gqa_set_path", "paged_gqa_last_plan",
@@ -58,6 +59,8 @@ def load(build_if_missing: bool = True):
             lib.paged_gqa_attn_ex.argtypes = [P, P, P, P, P, P, f, f, f, f, P, c_vp, ctypes.c_size_t, c_vp]
             lib.paged_gqa_attn_ex.restype = ctypes.c_int
             lib.paged_gqa_cache_write.argtypes = [P, P, P, P, P, P, P, f, f, c_vp]
+            lib.paged_gqa_attn_quant_q.restype = ctypes.c_int
+            lib.paged_gqa_attn_quant_q.argtypes = [P, P, P, P, P, P, f, f, f, P, c_vp]
             lib.paged_gqa_cache_write.restype = ctypes.c_int
             lib.paged_gqa_workspace_size.argtypes = [ctypes.c_int] * 7
             lib.paged_gqa_workspace_size.restype = ctypes.c_size_t
@@ -140,6 +143,17 @@ def paged_gqa_attn_ex(q, k_cache, v_cache, block_table, seq_lens, query_start_lo
     _check(lib.paged_gqa_attn_ex(*[ctypes.byref(x) for x in a], float(q_descale), float(k_descale),
                                  float(v_descale), float(softmax_scale), ctypes.byref(o), ptr, nbytes,
                                  _stream(stream)))
+
+
+def paged_gqa_attn_quant_q(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, k_descale: float,
+                           v_descale: float, softmax_scale: float, out, stream=None) -> None:
+    """paged_gqa_attn on a bf16 q quantised inside the call to e4m3 with one per-tensor scale."""
+    lib = load()
+    a = [_desc(q), _desc(k_cache), _desc(v_cache), _desc(block_table), _desc(seq_lens),
+         _desc(query_start_loc)]
+    o = _desc(out)
+    _check(lib.paged_gqa_attn_quant_q(*[ctypes.byref(x) for x in a], float(k_descale), float(v_descale),
+                                      float(softmax_scale), ctypes.byref(o), _stream(stream)))
 
 
 def paged_gqa_cache_write(k_new, v_new, k_cache, v_cache, block_table, seq_lens, query_start_loc,

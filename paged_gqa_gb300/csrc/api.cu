@@ -90,6 +90,7 @@ struct ClassSizes {
 struct WsLayout {
   ClassSizes cls[kNumClasses];
   size_t off[kNumClasses][8];
+  size_t q_amax_off;  // per-CTA maxima of |q| (calls that quantise Q)
   size_t total;
 };
 
@@ -128,6 +129,8 @@ WsLayout make_layout(int num_seqs, int T, int Hq, int Hkv, int sms) {
       at += align256(sz[i]);
     }
   }
+  L.q_amax_off = at;
+  at += align256(sizeof(float) * (size_t)q_amax_parts(sms));
   L.total = at;
   return L;
 }
@@ -169,7 +172,7 @@ int check_tensor(const pg_tensor* t, const char* name, int ndim) {
 
 int validate(const pg_tensor* q, const pg_tensor* k, const pg_tensor* v, const pg_tensor* bt,
              const pg_tensor* sl, const pg_tensor* qsl, float q_descale, float k_descale,
-             float v_descale, float softmax_scale, const pg_tensor* out, Validated* res) {
+             float v_descale, float softmax_scale, const pg_tensor* out, bool q_cast, Validated* res) {
   int st;
   if ((st = check_tensor(q, "q", 3)) || (st = check_tensor(k, "k_cache", 4)) ||
       (st = check_tensor(v, "v_cache", 4)) || (st = check_tensor(bt, "block_table", 2)) ||
@@ -185,6 +188,8 @@ int validate(const pg_tensor* q, const pg_tensor* k, const pg_tensor* v, const p
   if (q->dtype == PG_E4M3 && k->dtype != PG_E4M3)
     return fail(PG_ERR_UNSUPPORTED, "e4m3 q needs an e4m3 cache");
   if (out->dtype != PG_BF16) return fail(PG_ERR_UNSUPPORTED, "out must be bf16");
+  if (q_cast && (q->dtype != PG_BF16 || k->dtype != PG_E4M3))
+    return fail(PG_ERR_UNSUPPORTED, "quantising q needs a bf16 q and e4m3 caches");
   if (bt->dtype != PG_I32 || sl->dtype != PG_I32 || qsl->dtype != PG_I32)
     return fail(PG_ERR_INVALID_ARG, "block_table, seq_lens and query_start_loc must be int32");
   for (int i = 0; i < 4; ++i)
@@ -234,6 +239,8 @@ int validate(const pg_tensor* q, const pg_tensor* k, const pg_tensor* v, const p
   p.NB = (int)NB;
   p.q_is_fp8 = q->dtype == PG_E4M3;
   p.kv_is_fp8 = k->dtype == PG_E4M3;
+  p.q_cast = q_cast ? 1 : 0;
+  p.q_amax_parts = 0;
   p.q_st = q->stride[0];
   p.q_sh = q->stride[1];
   p.k_sb = k->stride[0];
@@ -256,6 +263,7 @@ int validate(const pg_tensor* q, const pg_tensor* k, const pg_tensor* v, const p
   ptr.qsl = static_cast<const int32_t*>(qsl->data);
   ptr.out = out->data;
   ptr.err = nullptr;
+  ptr.q_amax = nullptr;
   return PG_OK;
 }
 
@@ -268,12 +276,23 @@ int run(const Validated& val, const pg_tensor* k, const pg_tensor* v, void* ws, 
   for (int c = 0; c < kNumClasses; ++c) cp[c] = class_plan(L, c, static_cast<char*>(ws));
   (void)ws_bytes;
   int64_t plan_info[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  cudaError_t e = launch_plan(p, ptr, cp[0], cp[1], stream);
-  if (e != cudaSuccess) return cuda_fail(e, "plan launch");
-  int launched = 1;
   const int path = g_path.load();
   // Fast (tcgen05) kernels need an e4m3 cache; bf16 caches use the warp-MMA kernel.
   const bool fast_ok = path == 0 && p.kv_is_fp8;
+  // Only the tcgen05 kernels cast Q per tensor; nothing else may stand in for them.
+  if (p.q_cast && !fast_ok) return fail(PG_ERR_UNSUPPORTED, "quantising q needs the tcgen05 path");
+  int launched = 0;
+  cudaError_t e;
+  if (p.q_cast) {
+    p.q_amax_parts = q_amax_parts(ds->sms);
+    ptr.q_amax = reinterpret_cast<const float*>(static_cast<char*>(ws) + L.q_amax_off);
+    e = launch_q_amax(p, ptr, reinterpret_cast<float*>(static_cast<char*>(ws) + L.q_amax_off), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "q amax launch");
+    ++launched;
+  }
+  e = launch_plan(p, ptr, cp[0], cp[1], stream);
+  if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+  ++launched;
   int used = 0;
   for (int c = 0; c < kNumClasses; ++c) {
     bool done = false;
@@ -289,6 +308,7 @@ int run(const Validated& val, const pg_tensor* k, const pg_tensor* v, void* ws, 
         used |= 2 << c;
       }
     }
+    if (!done && p.q_cast) return fail(PG_ERR_UNSUPPORTED, "quantising q needs the tcgen05 path");
     if (!done) {
       e = launch_portable(p, ptr, cp[c], c == 0 ? kVerifyRows : kPrefillRows, stream);
       if (e != cudaSuccess) return cuda_fail(e, "portable kernel launch");
@@ -311,9 +331,9 @@ int run(const Validated& val, const pg_tensor* k, const pg_tensor* v, void* ws, 
 int attn_common(const pg_tensor* q, const pg_tensor* k, const pg_tensor* v, const pg_tensor* bt,
                 const pg_tensor* sl, const pg_tensor* qsl, float q_descale, float k_descale,
                 float v_descale, float softmax_scale, pg_tensor* out, void* user_ws,
-                size_t user_ws_bytes, bool use_user_ws, cudaStream_t stream) {
+                size_t user_ws_bytes, bool use_user_ws, cudaStream_t stream, bool q_cast = false) {
   Validated val;
-  int st = validate(q, k, v, bt, sl, qsl, q_descale, k_descale, v_descale, softmax_scale, out, &val);
+  int st = validate(q, k, v, bt, sl, qsl, q_descale, k_descale, v_descale, softmax_scale, out, q_cast, &val);
   if (st) return st;
   if (val.p.num_seqs == 0 || val.p.T == 0) {
     t_last_error.clear();
@@ -381,6 +401,15 @@ int paged_gqa_attn_ex(const pg_tensor* q, const pg_tensor* k_cache, const pg_ten
   return attn_common(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, q_descale, k_descale,
                      v_descale, softmax_scale, out, workspace, workspace_bytes, true,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+int paged_gqa_attn_quant_q(const pg_tensor* q, const pg_tensor* k_cache, const pg_tensor* v_cache,
+                           const pg_tensor* block_table, const pg_tensor* seq_lens,
+                           const pg_tensor* query_start_loc, float k_descale, float v_descale,
+                           float softmax_scale, pg_tensor* out, pg_stream_t stream) {
+  return attn_common(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, 1.0f, k_descale,
+                     v_descale, softmax_scale, out, nullptr, 0, false, reinterpret_cast<cudaStream_t>(stream),
+                     true);
 }
 
 size_t paged_gqa_workspace_size(int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
@@ -515,6 +544,7 @@ int paged_gqa_cache_write(const pg_tensor* k_new, const pg_tensor* v_new, const 
   a.T = (int)T;
   a.Hkv = (int)Hkv;
   a.P = (int)P;
+  a.p_shift = __builtin_ctz((unsigned)P);
   a.W = (int)W;
   a.NB = (int)NB;
   a.k_scale = 1.f / k_descale;

@@ -28,6 +28,11 @@ constexpr int kPrefillRows = 128;     // rows of a prefill block
 constexpr int kSlotRows = 128;        // rows per partial-result slot
 constexpr int kNumClasses = 2;        // 0 = verify, 1 = prefill
 
+// How a tcgen05 attention kernel stages Q (its template argument).
+constexpr int kQSplit = 0;  // bf16 Q as e4m3 hi + lo parts under a per-tile power-of-two scale
+constexpr int kQGiven = 1;  // e4m3 Q as given (its descale folded into the score scale)
+constexpr int kQCast = 2;   // bf16 Q cast to e4m3 with the call's per-tensor scale amax / 448
+
 // device error word bits
 constexpr uint32_t kErrBounds = 1u;   // qn > L, L > W*P, qsl not monotone
 constexpr uint32_t kErrPage = 2u;     // block-table entry outside [0, NB)
@@ -53,6 +58,8 @@ struct WorkItem {
 struct Problem {
   int num_seqs, T, Hq, Hkv, G, P, W, NB;
   int q_is_fp8, kv_is_fp8;
+  int q_cast;              // bf16 Q quantised per tensor inside the call (kQCast)
+  int q_amax_parts;        // entries of Pointers::q_amax (q_cast only)
   // strides in elements
   long long q_st, q_sh;
   long long k_sb, k_sp, k_sh;
@@ -72,6 +79,7 @@ struct Pointers {
   const int32_t* qsl;
   void* out;               // bf16
   uint32_t* err;           // device error word
+  const float* q_amax;     // per-CTA maxima of |q| from the amax kernel (q_cast only)
 };
 
 // Plan output in the workspace, one instance per class.

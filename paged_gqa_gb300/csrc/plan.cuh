@@ -20,11 +20,17 @@ struct CacheWriteArgs {
   const int32_t* seq_lens;
   const int32_t* qsl;
   int num_seqs, T, Hkv, P, W, NB;
+  int p_shift;             // log2(P)
   float k_scale, v_scale;  // 1 / descale
   uint32_t* err;
 };
 // Paged KV-cache write (cache_write.cu): new tokens' K and V -> e4m3 codes in their pages.
 cudaError_t launch_cache_write(const CacheWriteArgs& a, int sms, cudaStream_t stream);
+
+// Per-CTA maxima of |q| over a bf16 Q (q_amax.cu), q_amax_parts(sms) of them, for the
+// per-tensor cast of Q in the tcgen05 kernels.
+int q_amax_parts(int sms);
+cudaError_t launch_q_amax(const Problem& p, const Pointers& ptr, float* parts, cudaStream_t stream);
 
 // Warp-level MMA (mma.sync, tf32) kernel for one class's items; any dtype mix.
 cudaError_t launch_portable(const Problem& p, const Pointers& ptr, const ClassPlan& cp,

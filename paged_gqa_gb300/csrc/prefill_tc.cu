@@ -146,10 +146,12 @@ __device__ __forceinline__ void split4(float a, float b, float c, float d, uint3
 
 }  // namespace
 
-template <bool kQFp8>
+template <int kQM>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   Problem p, Pointers ptr, ClassPlan cp) {
+  constexpr bool kQFp8 = kQM != kQSplit;       // one e4m3 Q part in shared memory
+  constexpr int kQEsz = kQM == kQGiven ? 1 : 2;  // bytes of a Q element in HBM
   using LY = Layout<kQFp8>;
   constexpr int kVStages = LY::kVStages;
   extern __shared__ uint8_t smem_raw[];
@@ -341,6 +343,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     const int row = q4 * 32 + lane;        // TMEM lane = row of the block
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
     const int pair_bar = 1 + q4;           // named barrier of the two threads of each row
+    // {descale, 1/descale} of a per-tensor cast of Q (kQCast), the same in every thread
+    const float2 q_cast = kQM == kQCast ? q_cast_scales(ptr.q_amax, p.q_amax_parts, lane) : make_float2(1.f, 1.f);
     bool bad = false;
     float m_ref = kMInit, l = 0.f;
 
@@ -362,13 +366,35 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       auto src_of = [&](int r, int ch) -> const uint8_t* {
         const RowMap m = map_row(I.row0 + r, p.G, I.kvh);
         return static_cast<const uint8_t*>(ptr.q) +
-               ((size_t)(I.q0 + m.t) * p.q_st + (size_t)m.h * p.q_sh + ch * 16) * (kQFp8 ? 1 : 2);
+               ((size_t)(I.q0 + m.t) * p.q_st + (size_t)m.h * p.q_sh + ch * 16) * kQEsz;
       };
       auto dst_of = [&](int part, int r, int ch) -> uint8_t* {
         const int h = ch >> 3, c = ch & 7;
         return smem + LY::kOffQ + part * kQPart + h * kQHalf + r * 128 + ((c ^ (r & 7)) << 4);
       };
-      if (kQFp8) {
+      if (kQM == kQCast) {
+#pragma unroll
+        for (int k0 = 0; k0 < 8; k0 += 4) {
+          uint4 v[4][2];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int c = gi + (k0 + k) * kSoftThreads, r = c >> 4, ch = c & 15;
+            if (r < I.nrows) {
+              const uint4* s = reinterpret_cast<const uint4*>(src_of(r, ch));
+              v[k][0] = s[0];
+              v[k][1] = s[1];
+            } else {
+              v[k][0] = v[k][1] = make_uint4(0, 0, 0, 0);
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int c = gi + (k0 + k) * kSoftThreads, r = c >> 4, ch = c & 15;
+            *reinterpret_cast<uint4*>(dst_of(0, r, ch)) = bf16x16_to_e4m3(v[k][0], v[k][1], q_cast.y);
+          }
+        }
+        if (gi == 0) ms.qscale[pi] = q_cast.x;
+      } else if (kQM == kQGiven) {
 #pragma unroll
         for (int k0 = 0; k0 < 8; k0 += 4) {
           uint4 v[4];
@@ -630,9 +656,10 @@ int launch_prefill_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp
   int dev = 0;
   cudaGetDevice(&dev);
   cudaError_t e;
-  auto kern = p.q_is_fp8 ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
-  const size_t bytes = p.q_is_fp8 ? smem_bytes<true>() : smem_bytes<false>();
-  const int which = p.q_is_fp8 ? 2 : 1;
+  const int mode = p.q_cast ? kQCast : p.q_is_fp8 ? kQGiven : kQSplit;
+  auto kern = mode == kQCast ? prefill_tc_kernel<kQCast> : mode == kQGiven ? prefill_tc_kernel<kQGiven> : prefill_tc_kernel<kQSplit>;
+  const size_t bytes = mode != kQSplit ? smem_bytes<true>() : smem_bytes<false>();
+  const int which = 1 << mode;
   if (dev >= 0 && dev < 64 && !(attr_done[dev] & which)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) {

@@ -256,6 +256,31 @@ __device__ __forceinline__ void p_split4_f16(float x0, float x1, float x2, float
   s23 = *reinterpret_cast<__half2*>(&hb);
 }
 
+// The per-tensor e4m3 scale of a bf16 Q from the amax kernel's per-CTA maxima: descale =
+// amax / 448 and its reciprocal, each rounded to nearest in fp32; an amax of zero (or not
+// finite) takes descale = inv = 1. All lanes of the warp get the same pair {descale, inv}.
+__device__ __forceinline__ float2 q_cast_scales(const float* parts, int n, int lane) {
+  float a = 0.f;
+  for (int i = lane; i < n; i += 32) a = fmaxf(a, parts[i]);
+  a = warp_max(a);
+  if (!(a > 0.f) || !isfinite(a)) return make_float2(1.f, 1.f);
+  const float d = __fdiv_rn(a, 448.f);
+  return make_float2(d, __frcp_rn(d));
+}
+// 16 bf16 values (two uint4, element 0 first) times inv -> 16 e4m3 codes (uint4).
+__device__ __forceinline__ uint4 bf16x16_to_e4m3(uint4 a, uint4 b, float inv) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t u = w[2 * i], v = w[2 * i + 1];
+    c[i] = e4m3x2(__fmul_rn(__uint_as_float(u << 16), inv), __fmul_rn(__uint_as_float(u & 0xffff0000u), inv)) |
+           (e4m3x2(__fmul_rn(__uint_as_float(v << 16), inv), __fmul_rn(__uint_as_float(v & 0xffff0000u), inv))
+            << 16);
+  }
+  return make_uint4(c[0], c[1], c[2], c[3]);
+}
+
 // Two e4m3 codes (low byte first) -> two exact floats.
 __device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t v) {
   uint32_t h2;

@@ -97,9 +97,10 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
 
-template <bool kQFp8>
+template <int kQM>
 struct Shapes {
-  static constexpr int kSN = kQFp8 ? kVN : 2 * kVN;  // S MMA N: Q, or [Q_hi; Q_lo]
+  static constexpr int kSN = kQM != kQSplit ? kVN : 2 * kVN;  // S MMA N: Q, or [Q_hi; Q_lo]
+  static constexpr int kQEsz = kQM == kQGiven ? 1 : 2;        // bytes of a Q element in HBM
 };
 constexpr uint32_t kIdescO = idesc_e4m3(128, 2 * kVN, true, true);  // V^T (MN) x [P_hi; P_lo]^T (MN)
 
@@ -168,11 +169,12 @@ __device__ __forceinline__ void split4(float a, float b, float c, float d, uint3
 
 }  // namespace
 
-template <bool kQFp8>
+template <int kQM>
 __global__ void __launch_bounds__(kVThreads, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  Problem p, Pointers ptr, ClassPlan cp) {
-  constexpr int kSN = Shapes<kQFp8>::kSN;
+  constexpr int kSN = Shapes<kQM>::kSN;
+  constexpr int kQEsz = Shapes<kQM>::kQEsz;
   constexpr uint32_t kIdescS = idesc_e4m3(128, kSN, false, false);  // K (K-major) x Q (K-major)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -238,6 +240,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     const int q4 = warp & 3;                 // TMEM lane quarter
     const int c0 = (sw >> 2) * kCols;        // first row (column) this thread owns
     const int group_bar = 3 + (sw >> 2);     // named barrier of the row group's four warps
+    // {descale, 1/descale} of a per-tensor cast of Q (kQCast), the same in every thread
+    const float2 q_cast = kQM == kQCast ? q_cast_scales(ptr.q_amax, p.q_amax_parts, lane) : make_float2(1.f, 1.f);
     const int ti = q4 * 32 + lane;           // TMEM lane = key in tile = d in half
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
     float l[kCols];
@@ -267,14 +271,14 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       auto src_of = [&](int r, int ch) -> const uint8_t* {
         const RowMap m = map_row(I.row0 + r, p.G, I.kvh);
         return static_cast<const uint8_t*>(ptr.q) +
-               ((size_t)(I.q0 + m.t) * p.q_st + (size_t)m.h * p.q_sh + ch * 16) * (kQFp8 ? 1 : 2);
+               ((size_t)(I.q0 + m.t) * p.q_st + (size_t)m.h * p.q_sh + ch * 16) * kQEsz;
       };
       // part 0 = hi rows 0..63, part 1 = lo rows 64..127 of the stacked operand
       auto dst_of = [&](int part, int r, int ch) -> uint8_t* {
         const int h = ch >> 3, c = ch & 7, rr = part * kVN + r;
         return smem + kOffQ + h * kQHalf + rr * 128 + ((c ^ (rr & 7)) << 4);
       };
-      if (kQFp8) {
+      if (kQM == kQGiven) {
         uint4 v[kQChunks];
 #pragma unroll
         for (int k = 0; k < kQChunks; ++k) {
@@ -287,6 +291,25 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           *reinterpret_cast<uint4*>(dst_of(0, r, ch)) = v[k];
         }
         if (gi == 0) ms.qscale[pi] = 1.f;
+      } else if (kQM == kQCast) {
+        uint4 v[kQChunks][2];
+#pragma unroll
+        for (int k = 0; k < kQChunks; ++k) {
+          const int c = gi + k * kSoftThreads, r = c >> 4, ch = c & 15;
+          if (r < I.nrows) {
+            const uint4* s = reinterpret_cast<const uint4*>(src_of(r, ch));
+            v[k][0] = s[0];
+            v[k][1] = s[1];
+          } else {
+            v[k][0] = v[k][1] = make_uint4(0, 0, 0, 0);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kQChunks; ++k) {
+          const int c = gi + k * kSoftThreads, r = c >> 4, ch = c & 15;
+          *reinterpret_cast<uint4*>(dst_of(0, r, ch)) = bf16x16_to_e4m3(v[k][0], v[k][1], q_cast.y);
+        }
+        if (gi == 0) ms.qscale[pi] = q_cast.x;
       } else {
         uint4 v[kQChunks][2];
         float amax = 0.f;
@@ -350,7 +373,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         tmem_ld16(tmem + lane_addr + kColS + b * 128 + c0 + k, v);
 #pragma unroll
         for (int i = 0; i < 16; ++i) t[k + i] = v[i];
-        if (!kQFp8) {
+        if (kQM == kQSplit) {
           tmem_ld16(tmem + lane_addr + kColS + b * 128 + kVN + c0 + k, v);
 #pragma unroll
           for (int i = 0; i < 16; ++i) t[k + i] += v[i];
@@ -731,9 +754,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           for (int r = lane; r < I.nrows; r += 32) {
             const RowMap m = map_row(I.row0 + r, p.G, I.kvh);
             const uint8_t* row = static_cast<const uint8_t*>(ptr.q) +
-                                 ((size_t)(I.q0 + m.t) * p.q_st + (size_t)m.h * p.q_sh) * (kQFp8 ? 1 : 2);
+                                 ((size_t)(I.q0 + m.t) * p.q_st + (size_t)m.h * p.q_sh) * kQEsz;
 #pragma unroll
-            for (int c = 0; c < (kQFp8 ? 256 : 512); c += 128) prefetch_l2(row + c);
+            for (int c = 0; c < 256 * kQEsz; c += 128) prefetch_l2(row + c);
           }
         }
         const int32_t* bt_row = ptr.block_table + (size_t)I.seq * p.bt_stride;
@@ -873,8 +896,9 @@ int launch_verify_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp,
   int dev = 0;
   cudaGetDevice(&dev);
   cudaError_t e;
-  auto kern = p.q_is_fp8 ? verify_tc_kernel<true> : verify_tc_kernel<false>;
-  const int which = p.q_is_fp8 ? 2 : 1;
+  const int mode = p.q_cast ? kQCast : p.q_is_fp8 ? kQGiven : kQSplit;
+  auto kern = mode == kQCast ? verify_tc_kernel<kQCast> : mode == kQGiven ? verify_tc_kernel<kQGiven> : verify_tc_kernel<kQSplit>;
+  const int which = 1 << mode;
   if (dev >= 0 && dev < 64 && !(attr_done[dev] & which)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) {

@@ -158,3 +158,28 @@ def _cw_call(a, kd=1.0, vd=1.0):
 def test_cache_write_rejects_bad_arguments_before_any_launch(over, scales, code, msg):
     assert _cw_call(_cw_args(**over), *scales) == code
     assert msg in B.paged_gqa_last_error()
+
+
+def _qq_call(a, scale=1 / 16):
+    d = [B._desc(a[n]) for n in ("q", "k", "v", "bt", "sl", "qsl")]
+    o = B._desc(a["out"])
+    return pg.load().paged_gqa_attn_quant_q(*[ctypes.byref(x) for x in d], 1.0, 1.0, scale, ctypes.byref(o), None)
+
+
+@pytest.mark.parametrize("over,code,msg", [
+    (dict(q=FakeTensor((8, 16, 256), torch.uint8)), -2, "bf16 q"),
+    (dict(k=FakeTensor((10, 16, 1, 256), torch.bfloat16), v=FakeTensor((10, 16, 1, 256), torch.bfloat16)), -2,
+     "e4m3 caches"),
+    (dict(q=FakeTensor((8, 16, 128), torch.bfloat16)), -2, "head_dim"),
+    (dict(q=FakeTensor((8, 16, 256), torch.bfloat16, ptr=(1 << 20) + 2)), -1, "aligned"),
+])
+def test_quant_q_rejects_bad_arguments_before_any_launch(over, code, msg):
+    assert _qq_call(_args(**over)) == code
+    assert msg in pg.paged_gqa_last_error()
+
+
+def test_quant_q_empty_batch_is_a_no_op():
+    a = _args(bt=FakeTensor((0, 5), torch.int32), sl=FakeTensor((0,), torch.int32),
+              qsl=FakeTensor((1,), torch.int32), q=FakeTensor((0, 16, 256), torch.bfloat16),
+              out=FakeTensor((0, 16, 256), torch.bfloat16))
+    assert _qq_call(a) == 0

@@ -120,6 +120,12 @@ def config_spec(index: int, seed: int = 0) -> CaseSpec:
     raise ValueError(f"unknown config {index}")
 
 
+def write_chunks_spec() -> CaseSpec:
+    """A cache-write case that fits a profiler's memory budget but exceeds L2: 32 fresh
+    prefill chunks of 4096 tokens, 2 kv heads, 64-token pages (403 MB written and read)."""
+    return CaseSpec("write_chunks_b32_q4096_h2_p64", [(4096, 4096)] * 32, 16, 2, 64)
+
+
 def random_small_spec(gen: torch.Generator, *, group: int, num_kv_heads: int, page_size: int,
                       q_lens: Sequence[int], max_ctx: int, kv_dtype: str = "e4m3",
                       q_dtype: str = "bf16", spare_pages: int = 3, name: str = "small") -> CaseSpec:
