@@ -121,7 +121,7 @@ WsLayout make_layout(int num_seqs, int T, int Hq, int Hkv, int sms) {
         sizeof(RowBlock) * (size_t)s.max_blocks,                      // blocks
         sizeof(WorkItem) * (size_t)s.max_items,                       // items
         sizeof(int) * (size_t)s.max_blocks,                           // counters
-        sizeof(float) * (size_t)s.max_slots * s.slot_rows * kHeadDim, // part_o
+        sizeof(uint16_t) * (size_t)s.max_slots * s.slot_rows * kHeadDim, // part_o (f16)
         sizeof(float) * (size_t)s.max_slots * s.slot_rows,            // part_lse
         0};
     for (int i = 0; i < 8; ++i) {
@@ -145,7 +145,7 @@ ClassPlan class_plan(const WsLayout& L, int c, char* base) {
   cp.blocks = reinterpret_cast<RowBlock*>(base + o[2]);
   cp.items = reinterpret_cast<WorkItem*>(base + o[3]);
   cp.counters = reinterpret_cast<int*>(base + o[4]);
-  cp.part_o = reinterpret_cast<float*>(base + o[5]);
+  cp.part_o = reinterpret_cast<uint16_t*>(base + o[5]);
   cp.part_lse = reinterpret_cast<float*>(base + o[6]);
   cp.num_ctas = L.cls[c].num_ctas;
   cp.max_blocks = L.cls[c].max_blocks;

@@ -91,7 +91,8 @@ struct ClassPlan {
   RowBlock* blocks;        // [max_blocks]
   WorkItem* items;         // [max_items]
   int* counters;           // [max_blocks]
-  float* part_o;           // [max_slots][slot_rows][kHeadDim]
+  uint16_t* part_o;        // [max_slots][slot_rows][kHeadDim] f16: O / l in cache-code units
+                           // (v_descale is applied by the merge; |O / l| <= 448 fits f16)
   float* part_lse;         // [max_slots][slot_rows] (log2 units)
   int num_ctas;
   int max_blocks, max_items, max_slots;

@@ -51,8 +51,16 @@ __device__ __forceinline__ bool barrier_or(int id, int nthreads, bool pred) {
   return r != 0;
 }
 
-// Partial result slot of (block, split).
-__device__ __forceinline__ float* slot_o(const ClassPlan& cp, int slot) {
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+
+// Partial result slot of (block, split): f16 rows of O / l in cache-code units.
+__device__ __forceinline__ uint16_t* slot_o(const ClassPlan& cp, int slot) {
   return cp.part_o + (size_t)slot * cp.slot_rows * kHeadDim;
 }
 __device__ __forceinline__ float* slot_lse(const ClassPlan& cp, int slot) {
@@ -62,10 +70,11 @@ __device__ __forceinline__ float* slot_lse(const ClassPlan& cp, int slot) {
 constexpr int kMergeMaxSplits = 16;  // pieces whose weights fit the shared scratch
 
 // Called by `nthreads` threads (ids tid = 0..nthreads-1) that share barrier `bar_id`,
-// after each has written its share of this piece's partial result (normalised O and
-// log2-sum-exp per row) and executed __threadfence(). The last piece of a block to
-// arrive merges all pieces of the block:
-//     M = max_i lse_i,  w_i = 2^(lse_i - M) / sum_j 2^(lse_j - M),  out = sum_i w_i o_i
+// after each has written its share of this piece's partial result (normalised O in f16
+// code units and log2-sum-exp per row) and executed __threadfence(). The last piece of a
+// block to arrive merges all pieces of the block:
+//     M = max_i lse_i,  w_i = 2^(lse_i - M) / sum_j 2^(lse_j - M),
+//     out = v_descale * sum_i w_i o_i
 // ("Optimize Qwen3.5 MTP unified attention on gfx950": split-KV segments reduced by
 // a second pass). s_w is shared scratch of kMergeMaxSplits * kSlotRows floats.
 // Returns after the merge (if any) is complete.
@@ -101,7 +110,7 @@ __device__ inline void finish_split_block(const Problem& p, const Pointers& ptr,
         lse[i] = w;
         sum += w;
       }
-      const float inv = sum > 0.f ? 1.f / sum : 0.f;
+      const float inv = sum > 0.f ? p.out_scale / sum : 0.f;
 #pragma unroll
       for (int i = 0; i < kMergeMaxSplits; ++i)  // static indices keep lse[] in registers
         if (i < ns) s_w[i * kSlotRows + r] = lse[i] * inv;
@@ -114,12 +123,13 @@ __device__ inline void finish_split_block(const Problem& p, const Pointers& ptr,
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int i = 0; i < ns; ++i) {
         const float w = s_w[i * kSlotRows + r];
-        const float4 o = __ldcg(reinterpret_cast<const float4*>(slot_o(cp, rb.slot_base + i) +
-                                                                (size_t)r * kHeadDim + d));
-        acc.x += w * o.x;
-        acc.y += w * o.y;
-        acc.z += w * o.z;
-        acc.w += w * o.w;
+        const uint2 h = __ldcg(reinterpret_cast<const uint2*>(slot_o(cp, rb.slot_base + i) +
+                                                              (size_t)r * kHeadDim + d));
+        const float2 o01 = unpack_f16x2(h.x), o23 = unpack_f16x2(h.y);
+        acc.x += w * o01.x;
+        acc.y += w * o01.y;
+        acc.z += w * o23.x;
+        acc.w += w * o23.y;
       }
       const RowMap m = map_row(rb.row0 + r, p.G, rb.kvh);
       uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(ptr.out) +
@@ -138,13 +148,13 @@ __device__ inline void finish_split_block(const Problem& p, const Pointers& ptr,
     for (int i = 0; i < ns; ++i) {
       const float lse = __ldcg(slot_lse(cp, rb.slot_base + i) + r);
       const float w = (lse == -INFINITY) ? 0.f : exp2f(lse - M);
-      const float2 o = __ldcg(reinterpret_cast<const float2*>(slot_o(cp, rb.slot_base + i) +
-                                                              (size_t)r * kHeadDim + d));
+      const float2 o = unpack_f16x2(__ldcg(reinterpret_cast<const unsigned int*>(slot_o(cp, rb.slot_base + i) +
+                                                                                 (size_t)r * kHeadDim + d)));
       wsum += w;
       a0 += w * o.x;
       a1 += w * o.y;
     }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const float inv = wsum > 0.f ? p.out_scale / wsum : 0.f;
     const RowMap m = map_row(rb.row0 + r, p.G, rb.kvh);
     uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(ptr.out) +
                                                 (size_t)(seq_q0 + m.t) * p.o_st +

@@ -267,11 +267,13 @@ portable_attn_kernel(Problem p, Pointers ptr, ClassPlan cp) {
         for (int half = 0; half < 2; ++half) {
           const int lr = half ? lr1 : lr0;
           if (lr >= rb.nrows) continue;
-          float* dst = slot_o(cp, slot) + (size_t)lr * kHeadDim + 2 * tq;
-          const float inv = half ? inv1 : inv0;
+          uint16_t* dst = slot_o(cp, slot) + (size_t)lr * kHeadDim + 2 * tq;
+          // the partial leaves in code units: v_descale is applied by the merge
+          const float l = half ? l1 : l0;
+          const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
           for (int nd = 0; nd < 32; ++nd)
-            *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[nd][2 * half] * inv, o[nd][2 * half + 1] * inv);
+            *reinterpret_cast<uint32_t*>(dst + nd * 8) = pack_f16x2(o[nd][2 * half] * inv, o[nd][2 * half + 1] * inv);
           if (tq == 0) slot_lse(cp, slot)[lr] = half ? lse1 : lse0;
         }
       }

@@ -597,7 +597,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       const bool split = I.nsplit > 1;
       const int slot = I.slot_base + I.split;
       const bool valid = row < I.nrows;
-      const float inv = lr > 0.f ? p.out_scale / lr : 0.f;
+      // a split piece's partial stays in code units (v_descale is applied by the merge)
+      const float inv = lr > 0.f ? (split ? 1.f : p.out_scale) / lr : 0.f;
 #pragma unroll 1
       for (int k = 0; k < 128; k += 16) {
         float v[16];
@@ -606,10 +607,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         if (valid) {
           const int d = kh * 128 + k;
           if (split) {
-            float4* dst = reinterpret_cast<float4*>(slot_o(cp, slot) + (size_t)row * kHeadDim + d);
+            uint4* dst = reinterpret_cast<uint4*>(slot_o(cp, slot) + (size_t)row * kHeadDim + d);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+            for (int i = 0; i < 2; ++i)
+              dst[i] = make_uint4(pack_f16x2(v[8 * i] * inv, v[8 * i + 1] * inv),
+                                  pack_f16x2(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
+                                  pack_f16x2(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
+                                  pack_f16x2(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
           } else {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ptr.out) + ms.out_off[pi][row] + d);
 #pragma unroll

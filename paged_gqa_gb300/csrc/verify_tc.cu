@@ -113,6 +113,7 @@ struct Misc {
   alignas(16) int lim[2][kVN];
   alignas(16) long long out_off[2][kVN];
   alignas(16) float merge_w[kMergeMaxSplits * kSlotRows];
+  alignas(16) float lse_stage[kVN];  // a split piece's log2-sum-exp per row, for its bulk store
   alignas(8) uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[kPBufs], pv_done[kPBufs], q_full, q_free, o_ready, o_free, drain[2], merge_full;
@@ -559,53 +560,58 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         if ((lane & 1) == 0) ms.red[q4][c0 + (lane >> 1)] = v[0];
       }
       named_barrier(1, kSoftThreads);
+      const bool split = I.nsplit > 1;
+      // a split piece's partial stays in code units (v_descale is applied by the merge)
+      const float num = split ? 1.f : p.out_scale;
       float inv[kCols];
 #pragma unroll
       for (int n = 0; n < kCols; ++n) {
         const float lr = ms.red[0][c0 + n] + ms.red[1][c0 + n] + ms.red[2][c0 + n] + ms.red[3][c0 + n];
-        inv[n] = lr > 0.f ? __fdividef(p.out_scale, lr) : 0.f;
+        inv[n] = lr > 0.f ? __fdividef(num, lr) : 0.f;
       }
       float my_l = 0.f;  // row c0 + lane (lane < kCols), for the partial's log-sum-exp
       if (q4 == 0 && lane < kCols)
         my_l = ms.red[0][c0 + lane] + ms.red[1][c0 + lane] + ms.red[2][c0 + lane] + ms.red[3][c0 + lane];
       named_barrier(1, kSoftThreads);  // red is reused by the next item's first rescale
-      const bool split = I.nsplit > 1;
       const int slot = I.slot_base + I.split;
       if (split) {
-        // The fp32 partial (64 rows x 256) leaves in 16-row chunks through the P buffer
-        // (free: every P.V of the item has completed) by bulk stores, so these warps do not
-        // wait on thousands of scattered stores; the chunk rows of the slot are contiguous.
-        float* stage = reinterpret_cast<float*>(smem + kOffP);  // 16 rows x 256 floats
-        float* dst0 = slot_o(cp, slot);
-#pragma unroll
-        for (int r0 = 0; r0 < kVN; r0 += 16) {
-          if (r0 >= I.nrows) break;
-          if (c0 == r0 - r0 % kCols) {  // the warps that own rows r0 .. r0+15 (warp-uniform)
-            const int k = r0 % kCols;  // compile-time after unrolling: inv[] stays in registers
+        // The f16 partial (64 rows x 256 = 32 KB) and its log2-sum-exp per row leave through
+        // the P buffers (free: every P.V of the item has completed) by two bulk stores from
+        // one thread, so no warp waits on scattered stores and only that thread has global
+        // writes to complete before the block's split counter moves.
+        static_assert(kPBufs * kPBuf >= kVN * kHeadDim * 2, "the f16 partial fits the P buffers");
+        __half* stage = reinterpret_cast<__half*>(smem + kOffP);  // 64 rows x 256 halves
+        if (c0 < I.nrows) {  // warp-uniform
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-              float v[16], w[16];
-              tmem_ld16(tmem + lane_addr + kColO + h * 128 + c0 + k, v);
-              tmem_ld16(tmem + lane_addr + kColO + h * 128 + kVN + c0 + k, w);
-              tmem_wait_ld();
+          for (int h = 0; h < 2; ++h) {
+            float v[16], w[16];
+            tmem_ld16(tmem + lane_addr + kColO + h * 128 + c0, v);
+            tmem_ld16(tmem + lane_addr + kColO + h * 128 + kVN + c0, w);
+            tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) stage[i * kHeadDim + h * 128 + ti] = (v[i] + w[i]) * inv[k + i];
-            }
+            for (int i = 0; i < 16; ++i) stage[(c0 + i) * kHeadDim + h * 128 + ti] = __float2half_rn((v[i] + w[i]) * inv[i]);
           }
-          fence_proxy_async_smem();
-          named_barrier(1, kSoftThreads);
-          if (gi == 0) {
-            bulk_store(dst0 + (size_t)r0 * kHeadDim, smem_u32(stage), (uint32_t)min(16, I.nrows - r0) * kHeadDim * 4u);
-            bulk_commit();
-            bulk_wait_read_all();
-          }
-          named_barrier(1, kSoftThreads);
         }
-        // the partial is in global memory before the block's split counter moves
+        if (q4 == 0 && lane < kCols) {
+          const int row = c0 + lane;
+          ms.lse_stage[row] = my_l > 0.f ? ms.m[pi][row] - kSigma + log2f(my_l) : -INFINITY;
+        }
+        fence_proxy_async_smem();
+        named_barrier(1, kSoftThreads);
         if (gi == 0) {
-          bulk_wait_all();
+          bulk_store(slot_o(cp, slot), smem_u32(stage), (uint32_t)I.nrows * kHeadDim * 2u);
+          bulk_store(slot_lse(cp, slot), smem_u32(ms.lse_stage), kVN * 4u);  // all 64 entries of the slot
+          bulk_commit();
+          bulk_wait_all();  // the partial is in global memory before the split counter moves
           fence_proxy_async_global();
+          if (it + 1 == item_end && I.nsplit <= kMergeMaxSplits) {
+            // the CTA's last item: is this piece the block's last? (merged below)
+            __threadfence();
+            ms.merge_flag = atomicAdd(&cp.counters[I.block], 1) == I.nsplit - 1;
+            __threadfence();
+          }
         }
+        named_barrier(1, kSoftThreads);  // the stage is reused by the next item's P; merge_flag
       } else {
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
@@ -631,29 +637,16 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       tc_fence_before();
       mbar_arrive(bar(ms.o_free));
       if (split) {
-        if (q4 == 0 && lane < kCols && c0 + lane < I.nrows) {
-          const int row = c0 + lane;
-          slot_lse(cp, slot)[row] = my_l > 0.f ? ms.m[pi][row] - kSigma + log2f(my_l) : -INFINITY;
-        }
-        __threadfence();
         if (it + 1 == item_end && I.nsplit <= kMergeMaxSplits) {
-          // The CTA's last item: its K, V and P buffers are idle (every tile consumed, every
-          // MMA complete), so if this piece is the block's last, the merge bulk-loads the
-          // pieces' partials into them instead of reading them element by element (this
-          // merge is the tail of the kernel).
-          named_barrier(2, kSoftThreads);
-          if (gi == 0) {
-            __threadfence();
-            const int old = atomicAdd(&cp.counters[I.block], 1);
-            ms.merge_flag = old == I.nsplit - 1;
-            __threadfence();
-          }
-          named_barrier(2, kSoftThreads);
+          // The CTA's last item: its Q, K, V and P buffers are idle (every tile consumed,
+          // every MMA complete), so if this piece is the block's last, the merge bulk-loads
+          // the pieces' partials into them instead of reading them element by element (this
+          // merge is the tail of the kernel). The counter moved right after the partial left.
           if (ms.merge_flag) {
-            __threadfence();
+            // the counter's reader fenced after its atomic; the barrier orders the rest after it
             const int ns = I.nsplit;
-            constexpr uint32_t kRegion = kOffMisc - kOffK;  // K stages, V stages, P buffers
-            constexpr uint32_t kRowBytes = kHeadDim * 4;
+            constexpr uint32_t kRegion = kOffMisc - kOffQ;  // Q, K stages, V stages, P buffers
+            constexpr uint32_t kRowBytes = kHeadDim * 2;  // f16
             const int rpp = min(kVN, (int)(kRegion / (ns * kRowBytes)) / 8 * 8);  // rows per pass
             for (int r0 = 0; r0 < I.nrows; r0 += rpp) {
               const int nr = min(rpp, I.nrows - r0);
@@ -662,7 +655,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                 fence_proxy_async_smem();    // after the generic accesses to these buffers
                 mbar_expect_tx(bar(ms.merge_full), (uint32_t)(ns * nr) * kRowBytes);
                 for (int i = 0; i < ns; ++i)
-                  bulk_load(sbase + kOffK + (uint32_t)(i * rpp) * kRowBytes,
+                  bulk_load(sbase + kOffQ + (uint32_t)(i * rpp) * kRowBytes,
                             slot_o(cp, I.slot_base + i) + (size_t)r0 * kHeadDim, (uint32_t)nr * kRowBytes,
                             bar(ms.merge_full));
               }
@@ -682,7 +675,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                     lse[i] = lse[i] == -INFINITY ? 0.f : exp2f(lse[i] - M);
                     sum += lse[i];
                   }
-                  const float inv_sum = sum > 0.f ? 1.f / sum : 0.f;
+                  const float inv_sum = sum > 0.f ? p.out_scale / sum : 0.f;
 #pragma unroll
                   for (int i = 0; i < kMergeMaxSplits; ++i)
                     if (i < ns) ms.merge_w[i * kSlotRows + r] = lse[i] * inv_sum;
@@ -696,11 +689,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int i = 0; i < ns; ++i) {
                   const float w = ms.merge_w[i * kSlotRows + r0 + r];
-                  const float4 o = *reinterpret_cast<const float4*>(smem + kOffK + (size_t)(i * rpp + r) * kRowBytes + d * 4);
-                  acc.x += w * o.x;
-                  acc.y += w * o.y;
-                  acc.z += w * o.z;
-                  acc.w += w * o.w;
+                  const uint2 h = *reinterpret_cast<const uint2*>(smem + kOffQ + (size_t)(i * rpp + r) * kRowBytes + d * 2);
+                  const float2 o01 = unpack_f16x2(h.x), o23 = unpack_f16x2(h.y);
+                  acc.x += w * o01.x;
+                  acc.y += w * o01.y;
+                  acc.z += w * o23.x;
+                  acc.w += w * o23.y;
                 }
                 *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(ptr.out) + ms.out_off[pi][r0 + r] + d) =
                     make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
