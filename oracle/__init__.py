@@ -10,7 +10,9 @@ for the formula and the pages it follows). This module compiles it with gcc
 
 Parity status of every function here: pinned. The pins live in
 ``tests/test_oracle.py`` (brute-force dense attention, torch SDPA in fp64,
-closed forms, invariants, the FP8 table against torch.float8_e4m3fn).
+closed forms, invariants, the FP8 table against torch.float8_e4m3fn) and, for
+``sparse_attention``, ``tests/test_sparse_oracle.py`` (the dense oracle on full
+and compacted lists, order invariance, masking, duplicates, closed forms).
 """
 from __future__ import annotations
 
@@ -54,6 +56,15 @@ def _load():
                 P, I, L, L,            # q, q_dtype, q strides
                 P, P, I, L, L, L,      # k, v, kv_dtype, kv strides
                 P, L, P, P,            # block_table, stride, seq_lens, qsl
+                I, I, I, I, I, I,      # num_seqs, Hq, Hkv, D, P, NB
+                D, D, D, D,            # descales, softmax_scale
+                P, L, P, P, I]         # rows, nrows, out, lse, nthreads
+            lib.oracle_paged_gqa_sparse_attn.restype = ctypes.c_int
+            lib.oracle_paged_gqa_sparse_attn.argtypes = [
+                P, I, L, L,            # q, q_dtype, q strides
+                P, P, I, L, L, L,      # k, v, kv_dtype, kv strides
+                P, L, P, P,            # block_table, stride, seq_lens, qsl
+                P, L, L, I,            # indices, strides, K
                 I, I, I, I, I, I,      # num_seqs, Hq, Hkv, D, P, NB
                 D, D, D, D,            # descales, softmax_scale
                 P, L, P, P, I]         # rows, nrows, out, lse, nthreads
@@ -114,6 +125,44 @@ def attention(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, *,
         qn.ctypes.data, DTYPE_CODE[q_dtype], Hq * D, D,
         kn.ctypes.data, vn.ctypes.data, DTYPE_CODE[kv_dtype], P * Hkv * D, Hkv * D, D,
         bt.ctypes.data, bt_stride, sl.ctypes.data, qsl.ctypes.data,
+        num_seqs, Hq, Hkv, D, P, NB,
+        q_descale, k_descale, v_descale, softmax_scale,
+        rows.ctypes.data if rows is not None else None, rows.shape[0] if rows is not None else 0,
+        out.ctypes.data, lse.ctypes.data if lse is not None else None, int(threads))
+    if st != 0:
+        raise ValueError(f"oracle: {STATUS.get(st, st)}")
+    return (out, lse) if with_lse else out
+
+
+def sparse_attention(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, indices, *,
+                     q_dtype: str, kv_dtype: str, q_descale: float, k_descale: float,
+                     v_descale: float, softmax_scale: float, rows: Optional[np.ndarray] = None,
+                     threads: int = 0, with_lse: bool = False):
+    """fp64 sparse paged GQA attention: row (t, h) attends the entries of indices[t, h // G]
+    that lie in [0, its causal limit]; indices is [T, Hkv, K] int32 (see the C source)."""
+    lib = _load()
+    qn, kn, vn = _np(q), _np(k_cache), _np(v_cache)
+    bt = _np(block_table).astype(np.int32)
+    sl = _np(seq_lens).astype(np.int32)
+    qsl = _np(query_start_loc).astype(np.int32)
+    idx = np.ascontiguousarray(_np(indices).astype(np.int32))
+    T, Hq, D = q.shape
+    NB, P, Hkv, _ = k_cache.shape
+    K = idx.shape[2] if idx.ndim == 3 else 0
+    num_seqs = sl.shape[0]
+    if rows is not None:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        out = np.zeros((rows.shape[0], D), dtype=np.float64)
+        lse = np.zeros(rows.shape[0], dtype=np.float64) if with_lse else None
+    else:
+        out = np.zeros((T, Hq, D), dtype=np.float64)
+        lse = np.zeros((T, Hq), dtype=np.float64) if with_lse else None
+    bt_stride = bt.shape[1] if bt.ndim == 2 and bt.shape[1] > 0 else 1
+    st = lib.oracle_paged_gqa_sparse_attn(
+        qn.ctypes.data, DTYPE_CODE[q_dtype], Hq * D, D,
+        kn.ctypes.data, vn.ctypes.data, DTYPE_CODE[kv_dtype], P * Hkv * D, Hkv * D, D,
+        bt.ctypes.data, bt_stride, sl.ctypes.data, qsl.ctypes.data,
+        idx.ctypes.data, Hkv * K, K, K,
         num_seqs, Hq, Hkv, D, P, NB,
         q_descale, k_descale, v_descale, softmax_scale,
         rows.ctypes.data if rows is not None else None, rows.shape[0] if rows is not None else 0,

@@ -120,6 +120,47 @@ def config_spec(index: int, seed: int = 0) -> CaseSpec:
     raise ValueError(f"unknown config {index}")
 
 
+SPARSE_TOPK = 2051  # selected tokens per row in "Tune sparse GQA prefill profile on gfx942 and gfx950"
+
+
+def sparse_spec(tp: int = 1) -> CaseSpec:
+    """Sparse prefill: 8192 new tokens on a 32768-token context, 64-token pages, FP8 K/V,
+    bf16 Q; heads of the sparse page's TP1 (24 q / 2 kv) or TP2 (12 q / 1 kv) shapes."""
+    heads = {1: (24, 2), 2: (12, 1), 4: (6, 1), 8: (3, 1)}[tp]
+    return CaseSpec(f"sparse_prefill_q8192_L32768_h{heads[0]}x{heads[1]}_p64_top{SPARSE_TOPK}",
+                    [(8192, 32768)], heads[0], heads[1], 64)
+
+
+def sparse_indices(spec: CaseSpec, topk: int, device="cpu", seed: int = 0) -> torch.Tensor:
+    """[T, Hkv, topk] int32 selected positions per (token, kv head), ascending.
+
+    Row (t, h) of a sequence of length L with q_len qn sees positions 0..n-1, n = L - qn +
+    t + 1. If n <= topk it lists all of them and pads with -1; otherwise it takes one
+    position uniformly from each of topk strata [j n / topk, (j + 1) n / topk) (integer
+    bounds), so the positions are distinct and spread over the whole visible range.
+    Draws come from a generator on ``device`` seeded with seed + 11.
+    """
+    gen = _device_generator(device, seed + 11)
+    n_vis = []
+    for q, L in spec.seqs:
+        n_vis.append(torch.arange(L - q + 1, L + 1, dtype=torch.int64))
+    n = torch.cat(n_vis).to(device) if n_vis else torch.zeros(0, dtype=torch.int64, device=device)
+    T, H = n.shape[0], spec.num_kv_heads
+    j = torch.arange(topk, dtype=torch.int64, device=device)
+    out = torch.empty(T, H, topk, dtype=torch.int32, device=device)
+    chunk = max(1, (1 << 24) // max(1, H * topk))
+    for t0 in range(0, T, chunk):
+        nn = n[t0:t0 + chunk].view(-1, 1, 1)
+        lo = (j * nn) // topk
+        hi = ((j + 1) * nn) // topk
+        u = torch.rand(nn.shape[0], H, topk, generator=gen, device=device)
+        pos = lo + torch.minimum((u * (hi - lo)).to(torch.int64), hi - lo - 1)
+        full = nn <= topk
+        pos = torch.where(full, torch.where(j < nn, j, -1), pos)
+        out[t0:t0 + chunk] = pos.to(torch.int32)
+    return out
+
+
 def write_chunks_spec() -> CaseSpec:
     """A cache-write case that fits a profiler's memory budget but exceeds L2: 32 fresh
     prefill chunks of 4096 tokens, 2 kv heads, 64-token pages (403 MB written and read)."""
