@@ -21,6 +21,10 @@ bounded sample of the same workload on the host cores.
 --op attn_quant_q times paged_gqa_attn_quant_q: the same workload with its bf16 Q
 quantised inside the call to e4m3 under one per-tensor scale (amax / 448).
 
+--op sparse times paged_gqa_sparse_attn on the sparse prefill workload (8192 new tokens on
+a 32768-token context, 2051 selected positions per (token, kv head), heads of --sparse-tp):
+TFLOP/s of the used (row, key) pairs at 4 * 256 FLOPs each.
+
 --op cache_write times paged_gqa_cache_write instead: the config's new tokens (every
 sequence's last q_len positions, bf16 K and V for each kv head) quantised to e4m3 and
 scattered into their pages. Its value is GB/s of algorithmic bytes (per (token, kv head)
@@ -59,7 +63,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--op", default="attn", choices=["attn", "attn_quant_q", "cache_write"])
+    ap.add_argument("--op", default="attn", choices=["attn", "attn_quant_q", "cache_write", "sparse"])
+    ap.add_argument("--sparse-tp", type=int, default=1, choices=[1, 2, 4, 8],
+                    help="sparse: head layout of the sparse page's TP1/2/4/8 shapes")
     ap.add_argument("--write-case", default="config", choices=["config", "chunks"],
                     help="cache_write: the config's new tokens, or 32 fresh 4096-token chunks (profiling size)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
@@ -522,6 +528,177 @@ def run_cache_write_reference(args, rank, world):
             "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ---------------------------------------------------------------- sparse --
+
+SP_METRIC = "us/call and TFLOP/s of sparse paged GQA (used (row, key) pairs x 4 x 256)"
+
+
+def sp_used_pairs(spec, idx):
+    """(row, key) pairs the call uses: per (token, kv head) the entries in [0, causal
+    limit], times the kv head's G query heads."""
+    lim = torch.cat([torch.arange(L - q, L) for q, L in spec.seqs]).to(idx.device)
+    used = ((idx >= 0) & (idx <= lim.view(-1, 1, 1))).sum().item()
+    return int(used) * spec.group
+
+
+def sp_config(spec, tp, n, l2_note, used_pairs):
+    return {"workload": spec.name, "tp_shape": tp, "num_seqs": spec.num_seqs, "total_q": spec.total_q,
+            "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads, "head_dim": wl.HEAD_DIM,
+            "page_size": spec.page_size, "topk": wl.SPARSE_TOPK, "q_dtype": "bf16", "kv_dtype": "e4m3",
+            "used_pairs": used_pairs, "flops": used_pairs * 4 * wl.HEAD_DIM,
+            "gathered_kv_bytes": used_pairs // spec.group * 2 * wl.HEAD_DIM,
+            "parallelism": f"replicas{n}", "l2": l2_note, "seed": 0}
+
+
+def run_sparse(args, rank, world, local):
+    import paged_gqa_gb300 as pg
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg.load()
+    spec = wl.sparse_spec(args.sparse_tp)
+    case = wl.make_case(spec, device=dev, seed=rank)
+    idx = wl.sparse_indices(spec, wl.SPARSE_TOPK, device=dev, seed=rank)
+    used = sp_used_pairs(spec, idx)
+    flops = used * 4 * wl.HEAD_DIM
+    out = torch.empty(case.q.shape[0], case.q.shape[1], wl.HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def call(q=case.q, ix=idx, bt=case.block_table, sl=case.seq_lens, qsl=case.query_start_loc):
+        pg.paged_gqa_sparse_attn(q, case.k_cache, case.v_cache, bt, sl, qsl, ix, case.k_descale,
+                                 case.v_descale, case.softmax_scale, out)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    assert pg.paged_gqa_check_device_errors() == 0, pg.paged_gqa_last_error()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record()
+        call()  # one kernel per call: the events bracket that kernel alone
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    e2e = None
+    if not args.no_e2e:
+        src = (case.q, idx, case.block_table, case.seq_lens, case.query_start_loc)
+        host_in = [t.cpu().pin_memory() for t in src]
+        dev_in = [torch.empty_like(t) for t in src]
+        host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+
+        def e2e_step():
+            for h, d in zip(host_in, dev_in):
+                d.copy_(h, non_blocking=True)
+            call(dev_in[0], dev_in[1], dev_in[2], dev_in[3], dev_in[4])
+            host_out.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            flush.zero_()
+            e_ev[i][0].record()
+            e2e_step()
+            e_ev[i][1].record()
+        torch.cuda.synchronize()
+        e2e = (sum(a.elapsed_time(b) for a, b in e_ev) / K, h2d, host_out.numel() * host_out.element_size())
+    step_ms, e2e_ms = max_over_ranks([step_ms, e2e[0] if e2e else 0.0], world, dev)
+    if rank != 0:
+        return None
+    _, bf16, _, peak_src = load_peaks()
+    value = whole_job_value(flops / 1e12, world, step_ms)
+    achieved = flops / 1e12 / (step_ms / 1e3)
+    res = {
+        "metric": SP_METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "us_per_call": round(step_ms * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16 (e4m3 K/V, bf16 q)",
+        "data": "synthetic (seeded N(0,1) Q/K/V, FP8 per-tensor amax/448; stratified random top-k lists)",
+        "config": sp_config(spec, args.sparse_tp, world, "flushed: 512 MiB memset between timed calls", used),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16, "unit": "TFLOP/s",
+                     "frac": round(achieved / bf16, 4), "peak_source": f"{peak_src} (bf16_tflops burst; f16 dense = bf16)",
+                     "kernel": "sparse", "kernel_us": round(step_ms * 1e3, 2),
+                     "gathered_GBps": round(used // spec.group * 512 / 1e9 / (step_ms / 1e3), 1),
+                     "traffic": None},
+        "gpu_launches": K, "clocks": clocks, "wall_s": round(wall, 3),
+    }
+    if e2e:
+        res["e2e"] = {"value": round(flops * world / 1e12 / (e2e_ms / 1e3), 3), "unit": "TFLOP/s",
+                      "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2],
+                      "note": "per step: q, indices, block_table, seq_lens, query_start_loc H2D from pinned memory; out D2H; KV cache resident"}
+    if world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = sp_cpu_sample(spec, case, idx, used, args.cpu_seconds)
+    return res
+
+
+def sp_cpu_sample(spec, case, idx, used, target_s):
+    """The sparse oracle on growing random row samples until ~target_s; scaled by pairs."""
+    import numpy as np
+    import oracle
+    threads = oracle.max_threads()
+    c = wl.to_device(case, "cpu")
+    ix = idx.cpu()
+    lim = torch.cat([torch.arange(L - q, L) for q, L in spec.seqs])
+    per_row = ((ix >= 0) & (ix <= lim.view(-1, 1, 1))).sum(-1)  # [T, Hkv]
+    Hq, G = spec.num_q_heads, spec.group
+    gen = torch.Generator().manual_seed(4321)
+    n, elapsed, pairs, nrows = 16, 0.0, 0, 0
+    while elapsed < target_s:
+        rows = torch.randperm(spec.total_q * Hq, generator=gen)[:n].sort().values.numpy().astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.sparse_attention(c.q, c.k_cache, c.v_cache, c.block_table, c.seq_lens, c.query_start_loc, ix,
+                                q_dtype="bf16", kv_dtype="e4m3", q_descale=1.0, k_descale=case.k_descale,
+                                v_descale=case.v_descale, softmax_scale=spec.softmax_scale, rows=rows,
+                                threads=threads)
+        elapsed += time.perf_counter() - t0
+        r = torch.from_numpy(rows)
+        pairs += int(per_row[r // Hq, (r % Hq) // G].sum())
+        nrows += len(rows)
+        n = min(spec.total_q * Hq, n * 4)
+    est_s = elapsed * used / max(pairs, 1)
+    value = used * 4 * wl.HEAD_DIM / 1e12 / est_s
+    return {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{nrows} random (token, head) rows, {pairs} used (row, key) pairs in {elapsed:.1f} s; "
+                      f"scaled by the workload's {used} pairs",
+            "est_full_s": round(est_s, 6), "sample_s": round(elapsed, 6)}
+
+
+def run_sparse_reference(args, rank, world):
+    if rank != 0:
+        return None
+    spec = wl.sparse_spec(args.sparse_tp)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    case = wl.make_case(spec, device=dev, seed=0)
+    idx = wl.sparse_indices(spec, wl.SPARSE_TOPK, device=dev, seed=0)
+    used = sp_used_pairs(spec, idx)
+    per = max(1.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        sp_cpu_sample(spec, case, idx, used, per / 4)
+    runs = [sp_cpu_sample(spec, case, idx, used, per) for _ in range(args.steps)]
+    value = statistics.median(r["value"] for r in runs)
+    est_s = statistics.median(r["est_full_s"] for r in runs)
+    return {"impl": "reference", "metric": SP_METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(est_s * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) Q/K/V, FP8 per-tensor amax/448; stratified random top-k lists)",
+            "config": sp_config(spec, args.sparse_tp, world, "n/a (CPU)", used),
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": runs[-1]["cores"], "kind": "oracle",
+                             "sample": runs[-1]["sample"]},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 # ------------------------------------------------------------------- oracle --
 
 def _oracle_sample(spec, case, target_s, kind, quant_q=False):
@@ -632,9 +809,10 @@ def main():
     if world > 1 and args.impl == "ours":
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     if args.impl == "reference":
-        res = (run_cache_write_reference if args.op == "cache_write" else run_reference)(args, rank, world)
+        res = {"cache_write": run_cache_write_reference, "sparse": run_sparse_reference}.get(
+            args.op, run_reference)(args, rank, world)
     else:
-        res = (run_cache_write if args.op == "cache_write" else run_ours)(args, rank, world, local)
+        res = {"cache_write": run_cache_write, "sparse": run_sparse}.get(args.op, run_ours)(args, rank, world, local)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1 and args.impl == "ours":

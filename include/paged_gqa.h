@@ -167,6 +167,28 @@ int paged_gqa_attn_quant_q(const pg_tensor* q, const pg_tensor* k_cache, const p
                            float softmax_scale, pg_tensor* out, pg_stream_t stream);
 
 /*
+ * paged_gqa_sparse_attn -- sparse paged GQA attention ("Tune sparse GQA prefill profile on
+ * gfx942 and gfx950": each query row attends a selected list of tokens, ~2k per row,
+ * head_dim 256, FP8 K/V). Row (token t, q head h) attends the keys listed in
+ * indices[t, h / G, :]: for each entry p with 0 <= p <= L - q_len + (t - q_start) (the
+ * row's bottom-right causal limit) the key at position p of t's sequence (page
+ * block_table[s][p / P], slot p mod P) takes part in the softmax; other entries (negative,
+ * or past the limit) are not used; an entry listed twice counts twice. A row with no
+ * used entry is written as zeros.
+ *
+ * Arguments as paged_gqa_attn, plus
+ *   indices  [T, num_kv_heads, K] int32 positions, last dim contiguous, 4-byte aligned;
+ *            K may be 0 (every row zero). Caller-owned, read only.
+ * q must be bf16 and the caches e4m3 with the same strides (else PG_ERR_UNSUPPORTED /
+ * PG_ERR_INVALID_ARG). Allocates nothing. A block-table entry out of range sets
+ * PG_ERR_DEVICE_BOUNDS in the device error word and the key is skipped.
+ */
+int paged_gqa_sparse_attn(const pg_tensor* q, const pg_tensor* k_cache, const pg_tensor* v_cache,
+                          const pg_tensor* block_table, const pg_tensor* seq_lens,
+                          const pg_tensor* query_start_loc, const pg_tensor* indices, float k_descale,
+                          float v_descale, float softmax_scale, pg_tensor* out, pg_stream_t stream);
+
+/*
  * paged_gqa_cache_write -- the step before the call: write the new tokens' K and V into
  * the paged FP8 cache it reads ("Optimize Qwen3.5 MTP unified attention on gfx950" and
  * "asm FP8 FMHA for prefix-hit prefill" read such a cache; this fills it).

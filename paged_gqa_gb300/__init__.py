@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     paged_gqa_attn,
     paged_gqa_attn_ex,
     paged_gqa_attn_quant_q,
+    paged_gqa_sparse_attn,
     paged_gqa_cache_write,
     paged_gqa_check_device_errors,
     paged_gqa_last_error,

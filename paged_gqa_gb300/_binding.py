@@ -16,7 +16,7 @@ STATUS_NAMES = {0: "PG_OK", -1: "PG_ERR_INVALID_ARG", -2: "PG_ERR_UNSUPPORTED", 
 
 # Every symbol include/paged_gqa.h declares.
 EXPORTED = ("paged_gqa_attn", "paged_gqa_attn_ex", "paged_gqa_attn_noalloc", "paged_gqa_attn_quant_q",
-            "paged_gqa_cache_write",
+            "paged_gqa_sparse_attn", "paged_gqa_cache_write",
             "paged_gqa_workspace_size",
             "paged_gqa_last_error",
             "paged_gqa_check_device_errors", "paged_gqa_set_path", "paged_gqa_last_plan",
@@ -61,6 +61,8 @@ def load(build_if_missing: bool = True):
             lib.paged_gqa_cache_write.argtypes = [P, P, P, P, P, P, P, f, f, c_vp]
             lib.paged_gqa_attn_quant_q.restype = ctypes.c_int
             lib.paged_gqa_attn_quant_q.argtypes = [P, P, P, P, P, P, f, f, f, P, c_vp]
+            lib.paged_gqa_sparse_attn.restype = ctypes.c_int
+            lib.paged_gqa_sparse_attn.argtypes = [P, P, P, P, P, P, P, f, f, f, P, c_vp]
             lib.paged_gqa_cache_write.restype = ctypes.c_int
             lib.paged_gqa_workspace_size.argtypes = [ctypes.c_int] * 7
             lib.paged_gqa_workspace_size.restype = ctypes.c_size_t
@@ -154,6 +156,17 @@ def paged_gqa_attn_quant_q(q, k_cache, v_cache, block_table, seq_lens, query_sta
     o = _desc(out)
     _check(lib.paged_gqa_attn_quant_q(*[ctypes.byref(x) for x in a], float(k_descale), float(v_descale),
                                       float(softmax_scale), ctypes.byref(o), _stream(stream)))
+
+
+def paged_gqa_sparse_attn(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, indices,
+                          k_descale: float, v_descale: float, softmax_scale: float, out, stream=None) -> None:
+    """Sparse paged GQA attention: row (t, h) attends the listed positions indices[t, h // G]."""
+    lib = load()
+    a = [_desc(q), _desc(k_cache), _desc(v_cache), _desc(block_table), _desc(seq_lens),
+         _desc(query_start_loc), _desc(indices)]
+    o = _desc(out)
+    _check(lib.paged_gqa_sparse_attn(*[ctypes.byref(x) for x in a], float(k_descale), float(v_descale),
+                                     float(softmax_scale), ctypes.byref(o), _stream(stream)))
 
 
 def paged_gqa_cache_write(k_new, v_new, k_cache, v_cache, block_table, seq_lens, query_start_loc,

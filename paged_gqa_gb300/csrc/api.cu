@@ -412,6 +412,77 @@ int paged_gqa_attn_quant_q(const pg_tensor* q, const pg_tensor* k_cache, const p
                      true);
 }
 
+int paged_gqa_sparse_attn(const pg_tensor* q, const pg_tensor* k_cache, const pg_tensor* v_cache,
+                          const pg_tensor* block_table, const pg_tensor* seq_lens,
+                          const pg_tensor* query_start_loc, const pg_tensor* indices, float k_descale,
+                          float v_descale, float softmax_scale, pg_tensor* out, pg_stream_t stream) {
+  Validated val;
+  int st = validate(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, 1.0f, k_descale, v_descale,
+                    softmax_scale, out, false, &val);
+  if (st) return st;
+  if ((st = check_tensor(indices, "indices", 3))) return st;
+  if (q->dtype != PG_BF16 || k_cache->dtype != PG_E4M3)
+    return fail(PG_ERR_UNSUPPORTED, "sparse attention takes a bf16 q and e4m3 caches");
+  for (int i = 0; i < 3; ++i)
+    if (k_cache->stride[i] != v_cache->stride[i])
+      return fail(PG_ERR_INVALID_ARG, "sparse attention needs k_cache and v_cache with the same strides");
+  const Problem& p = val.p;
+  if (indices->dtype != PG_I32) return fail(PG_ERR_INVALID_ARG, "indices must be int32");
+  if (indices->shape[0] != p.T || indices->shape[1] != p.Hkv)
+    return fail(PG_ERR_INVALID_ARG, "indices must be [T, num_kv_heads, K]");
+  const long long K = indices->shape[2];
+  if (K > INT32_MAX / 2) return fail(PG_ERR_UNSUPPORTED, "sizes beyond the supported range");
+  if (K > 1 && indices->stride[2] != 1) return fail(PG_ERR_INVALID_ARG, "indices rows must be contiguous");
+  if (K > 0 && p.T > 0 && (!indices->data || (reinterpret_cast<uintptr_t>(indices->data) & 3u)))
+    return fail(PG_ERR_INVALID_ARG, "indices must be non-null and 4-byte aligned");
+  if (p.num_seqs == 0 || p.T == 0) {
+    t_last_error.clear();
+    return PG_OK;
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceState* ds = nullptr;
+  if ((st = device_state(dev, &ds)) != PG_OK) return st;
+  SparseArgs a;
+  a.q = static_cast<const uint16_t*>(q->data);
+  a.q_st = p.q_st;
+  a.q_sh = p.q_sh;
+  a.k = static_cast<const uint8_t*>(k_cache->data);
+  a.v = static_cast<const uint8_t*>(v_cache->data);
+  a.kv_sb = p.k_sb;
+  a.kv_sp = p.k_sp;
+  a.kv_sh = p.k_sh;
+  a.bt = val.ptr.block_table;
+  a.bt_stride = p.bt_stride;
+  a.seq_lens = val.ptr.seq_lens;
+  a.qsl = val.ptr.qsl;
+  a.idx = static_cast<const int32_t*>(indices->data);
+  a.idx_st = indices->stride[0];
+  a.idx_sh = indices->stride[1];
+  a.K = (int)K;
+  a.out = static_cast<uint16_t*>(out->data);
+  a.o_st = p.o_st;
+  a.o_sh = p.o_sh;
+  a.num_seqs = p.num_seqs;
+  a.T = p.T;
+  a.Hq = p.Hq;
+  a.Hkv = p.Hkv;
+  a.G = p.G;
+  a.HG = (p.G + 15) / 16;
+  a.P = p.P;
+  a.p_shift = __builtin_ctz((unsigned)p.P);
+  a.W = p.W;
+  a.NB = p.NB;
+  a.score_scale_log2 = (float)((double)softmax_scale * (double)k_descale * 1.4426950408889634);
+  a.out_scale = v_descale;
+  a.err = ds->err;
+  e = launch_sparse(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");
+  t_last_error.clear();
+  return PG_OK;
+}
+
 size_t paged_gqa_workspace_size(int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
                                 int page_size, int max_blocks_per_seq, int device) {
   (void)max_blocks_per_seq;

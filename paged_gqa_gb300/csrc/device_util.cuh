@@ -67,6 +67,28 @@ __device__ __forceinline__ float* slot_lse(const ClassPlan& cp, int slot) {
   return cp.part_lse + (size_t)slot * cp.slot_rows;
 }
 
+// The sequence of token t: the last s in [0, n) with qsl[s] <= t (0 if none), found by a
+// 32-way search: each step the warp probes 32 points of the remaining interval at once, so
+// a batch of n sequences takes about log32(n) dependent loads. Every lane gets the answer;
+// the warp must be converged. A query_start_loc that is not monotone still yields an index
+// in [0, n); the caller's range check on the token then flags it.
+__device__ __forceinline__ int seq_of_token(const int32_t* qsl, int n, int t, int lane) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int span = hi - lo;
+    const int p = lo + (int)(((long long)(lane + 1) * span + 31) / 32);  // in (lo, hi]; lane 31: hi
+    const unsigned m = __ballot_sync(0xffffffffu, __ldg(qsl + p) <= t);
+    if (m == 0) {
+      hi = __shfl_sync(0xffffffffu, p, 0) - 1;
+    } else {
+      const int k = 31 - __clz((int)m);  // the last probe at or below t
+      lo = __shfl_sync(0xffffffffu, p, k);
+      if (k < 31) hi = min(hi, __shfl_sync(0xffffffffu, p, k + 1) - 1);
+    }
+  }
+  return lo;
+}
+
 constexpr int kMergeMaxSplits = 16;  // pieces whose weights fit the shared scratch
 
 // Called by `nthreads` threads (ids tid = 0..nthreads-1) that share barrier `bar_id`,

@@ -27,6 +27,29 @@ struct CacheWriteArgs {
 // Paged KV-cache write (cache_write.cu): new tokens' K and V -> e4m3 codes in their pages.
 cudaError_t launch_cache_write(const CacheWriteArgs& a, int sms, cudaStream_t stream);
 
+// Arguments of sparse paged GQA attention (sparse.cu).
+struct SparseArgs {
+  const uint16_t* q;                   // [T, Hq, 256] bf16
+  long long q_st, q_sh;                // elements
+  const uint8_t* k;                    // [NB, P, Hkv, 256] e4m3
+  const uint8_t* v;
+  long long kv_sb, kv_sp, kv_sh;       // bytes, the same for K and V
+  const int32_t* bt;
+  long long bt_stride;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  const int32_t* idx;                  // [T, Hkv, K] positions
+  long long idx_st, idx_sh;            // elements
+  int K;
+  uint16_t* out;                       // [T, Hq, 256] bf16
+  long long o_st, o_sh;                // elements
+  int num_seqs, T, Hq, Hkv, G, HG, P, p_shift, W, NB;  // HG = ceil(G / 16) head groups per kv head
+  float score_scale_log2;              // softmax_scale * k_descale * log2(e)
+  float out_scale;                     // v_descale
+  uint32_t* err;
+};
+cudaError_t launch_sparse(const SparseArgs& a, cudaStream_t stream);
+
 // Per-CTA maxima of |q| over a bf16 Q (q_amax.cu), q_amax_parts(sms) of them, for the
 // per-tensor cast of Q in the tcgen05 kernels.
 int q_amax_parts(int sms);

@@ -183,3 +183,25 @@ def test_quant_q_empty_batch_is_a_no_op():
               qsl=FakeTensor((1,), torch.int32), q=FakeTensor((0, 16, 256), torch.bfloat16),
               out=FakeTensor((0, 16, 256), torch.bfloat16))
     assert _qq_call(a) == 0
+
+
+def _sp_call(a, idx):
+    d = [B._desc(a[n]) for n in ("q", "k", "v", "bt", "sl", "qsl")] + [B._desc(idx)]
+    o = B._desc(a["out"])
+    return pg.load().paged_gqa_sparse_attn(*[ctypes.byref(x) for x in d], 1.0, 1.0, 1 / 16, ctypes.byref(o), None)
+
+
+@pytest.mark.parametrize("over,idx,code,msg", [
+    (dict(q=FakeTensor((8, 16, 256), torch.uint8)), FakeTensor((8, 1, 64), torch.int32), -2, "bf16 q"),
+    (dict(k=FakeTensor((10, 16, 1, 256), torch.bfloat16), v=FakeTensor((10, 16, 1, 256), torch.bfloat16)),
+     FakeTensor((8, 1, 64), torch.int32), -2, "e4m3 caches"),
+    (dict(v=FakeTensor((10, 16, 1, 256), torch.uint8, stride=[8192, 512, 512, 1])),
+     FakeTensor((8, 1, 64), torch.int32), -1, "same strides"),
+    ({}, FakeTensor((8, 2, 64), torch.int32), -1, "[T, num_kv_heads, K]"),
+    ({}, FakeTensor((8, 1, 64), torch.float32), -1, "int32"),
+    ({}, FakeTensor((8, 1, 64), torch.int32, stride=[128, 128, 2]), -1, "contiguous"),
+    ({}, FakeTensor((8, 1, 64), torch.int32, ptr=(1 << 20) + 2), -1, "aligned"),
+])
+def test_sparse_rejects_bad_arguments_before_any_launch(over, idx, code, msg):
+    assert _sp_call(_args(**over), idx) == code
+    assert msg in pg.paged_gqa_last_error()

@@ -1,0 +1,126 @@
+"""Sparse paged GQA on the GPU against the oracle, element by element."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(case, idx, out=None, check=True):
+    import paged_gqa_gb300 as pg
+    T, Hq = case.q.shape[0], case.q.shape[1]
+    if out is None:
+        out = torch.full((T, Hq, wl.HEAD_DIM), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pg.paged_gqa_sparse_attn(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                             case.query_start_loc, idx, case.k_descale, case.v_descale, case.softmax_scale, out)
+    if check:
+        assert pg.paged_gqa_check_device_errors() == 0, pg.paged_gqa_last_error()
+    return out
+
+
+def _oracle(case, idx, rows=None):
+    c = gu.to_device(case, "cpu")
+    return oracle.sparse_attention(c.q, c.k_cache, c.v_cache, c.block_table, c.seq_lens, c.query_start_loc,
+                                   idx.cpu(), q_dtype="bf16", kv_dtype="e4m3", q_descale=1.0,
+                                   k_descale=case.k_descale, v_descale=case.v_descale,
+                                   softmax_scale=case.spec.softmax_scale, rows=rows)
+
+
+def _random_lists(case, K, seed, junk=True):
+    """Random positions in [-3, L + 5) per (token, kv head): in-range, padding, past the
+    causal limit, and duplicates all occur."""
+    g = torch.Generator().manual_seed(seed)
+    T, Hkv = case.q.shape[0], case.spec.num_kv_heads
+    Lmax = int(case.seq_lens.max())
+    lo = -3 if junk else 0
+    idx = torch.randint(lo, Lmax + (5 if junk else 0), (T, Hkv, K), generator=g, dtype=torch.int32)
+    if K >= 4:
+        idx[:, :, 1] = idx[:, :, 0]  # a duplicate in every list
+    return idx.cuda()
+
+
+SMALL = [
+    # (group, kv heads, page, q_lens, max context, K)
+    (12, 2, 64, [4, 1, 37], 500, 100),     # the sparse page's TP1 head layout, ragged K
+    (12, 1, 16, [9, 2], 300, 33),          # TP2
+    (6, 1, 32, [5, 16], 200, 64),          # TP4
+    (3, 1, 16, [7], 90, 5),                # TP8, a short list
+    (16, 1, 64, [3, 20], 400, 70),         # a full 16-head group
+    (24, 1, 16, [6, 2], 250, 40),          # two head groups per kv head
+]
+
+
+@pytest.mark.parametrize("i", range(len(SMALL)))
+def test_small_cases_match_the_oracle(i):
+    G, hkv, page, q_lens, ctx, K = SMALL[i]
+    gen = torch.Generator().manual_seed(90 + i)
+    spec = wl.random_small_spec(gen, group=G, num_kv_heads=hkv, page_size=page, q_lens=q_lens, max_ctx=ctx,
+                                kv_dtype="e4m3", q_dtype="bf16")
+    case = wl.make_case(spec, device="cuda", seed=90 + i, poison=True)
+    idx = _random_lists(case, K, 90 + i)
+    gu.compare(_run(case, idx), _oracle(case, idx), f"sparse case {i}")
+
+
+def test_generated_top_k_lists_and_empty_lists():
+    gen = torch.Generator().manual_seed(97)
+    spec = wl.random_small_spec(gen, group=12, num_kv_heads=2, page_size=64, q_lens=[40, 3], max_ctx=900,
+                                kv_dtype="e4m3", q_dtype="bf16")
+    case = wl.make_case(spec, device="cuda", seed=97, poison=True)
+    idx = wl.sparse_indices(case.spec, 129, device="cuda", seed=97)
+    gu.compare(_run(case, idx), _oracle(case, idx), "generated top-k lists")
+    none = torch.full_like(idx, -1)
+    out = _run(case, none)
+    assert (out == 0).all()
+    empty = torch.empty(idx.shape[0], idx.shape[1], 0, dtype=torch.int32, device="cuda")
+    assert (_run(case, empty) == 0).all()
+
+
+def test_full_lists_equal_the_dense_call():
+    """Listing every position 0..L-1 is the dense attention: the sparse kernel against the
+    dense oracle and against the dense GPU path on the same case."""
+    gen = torch.Generator().manual_seed(98)
+    spec = wl.random_small_spec(gen, group=12, num_kv_heads=1, page_size=16, q_lens=[4, 130], max_ctx=600,
+                                kv_dtype="e4m3", q_dtype="bf16")
+    case = wl.make_case(spec, device="cuda", seed=98, poison=True)
+    Lmax = int(case.seq_lens.max())
+    idx = torch.arange(Lmax, dtype=torch.int32, device="cuda").expand(case.q.shape[0], 1, Lmax).contiguous()
+    got = _run(case, idx)
+    gu.check_full(case, got, "full lists vs dense oracle")
+    dense = gu.run_library(case)
+    assert (got.float() - dense.float()).abs().max().item() < 1e-2
+
+
+def test_bad_page_is_flagged_and_the_key_skipped():
+    import paged_gqa_gb300 as pg
+    gen = torch.Generator().manual_seed(99)
+    spec = wl.random_small_spec(gen, group=6, num_kv_heads=1, page_size=16, q_lens=[3], max_ctx=200,
+                                kv_dtype="e4m3", q_dtype="bf16")
+    case = wl.make_case(spec, device="cuda", seed=99)
+    idx = wl.sparse_indices(case.spec, 20, device="cuda", seed=99)
+    bt = case.block_table.clone()
+    bt[0, 0] = case.num_blocks + 7  # page of positions 0..15: out of range
+    case_bad = wl.Case(case.spec, case.q, case.k_cache, case.v_cache, bt, case.seq_lens, case.query_start_loc,
+                       case.q_descale, case.k_descale, case.v_descale, case.softmax_scale)
+    got = _run(case_bad, idx, check=False)
+    assert pg.paged_gqa_check_device_errors() == -5
+    dropped = torch.where(idx < 16, torch.full_like(idx, -1), idx)  # what the kernel skipped
+    gu.compare(got, _oracle(case, dropped), "bad page skipped")
+
+
+def test_sparse_prefill_workload_sampled_rows():
+    """The sparse page's TP1 shape: 8192 new tokens on a 32768-token context, 24 q / 2 kv
+    heads, 2051 selected positions per (token, kv head); sampled rows and the end tokens."""
+    spec = wl.sparse_spec(1)
+    case = wl.make_case(spec, device="cuda", seed=0, poison=True)
+    idx = wl.sparse_indices(spec, wl.SPARSE_TOPK, device="cuda", seed=0)
+    got = _run(case, idx).reshape(-1, wl.HEAD_DIM)
+    Hq = spec.num_q_heads
+    gen = torch.Generator().manual_seed(1)
+    rows = torch.cat([torch.arange(Hq), torch.randperm(spec.total_q * Hq, generator=gen)[:400],
+                      torch.arange((spec.total_q - 1) * Hq, spec.total_q * Hq)]).numpy().astype(np.int64)
+    ref = _oracle(case, idx, rows=rows)
+    gu.compare(got[torch.from_numpy(rows).cuda()], ref, "sparse prefill TP1 sampled rows")
