@@ -136,14 +136,6 @@ __device__ __forceinline__ float2 bf2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-__device__ __forceinline__ void split4(float a, float b, float c, float d, uint32_t& hi, uint32_t& lo) {
-  const uint32_t h01 = e4m3x2(a, b), h23 = e4m3x2(c, d);
-  const float2 f01 = e4m3x2_to_f2(h01), f23 = e4m3x2_to_f2(h23);
-  const uint32_t l01 = e4m3x2(a - f01.x, b - f01.y), l23 = e4m3x2(c - f23.x, d - f23.y);
-  hi = h01 | (h23 << 16);
-  lo = l01 | (l23 << 16);
-}
-
 }  // namespace
 
 template <int kQM>
