@@ -18,8 +18,9 @@ slowest rank's time.
 --impl reference times the fp64 CPU oracle (the only reference this path has) on a
 bounded sample of the same workload on the host cores.
 
---op attn_quant_q times paged_gqa_attn_quant_q: the same workload with its bf16 Q
-quantised inside the call to e4m3 under one per-tensor scale (amax / 448).
+--op attn_quant_q times paged_gqa_attn_quant_q: the same workload with its Q given in bf16
+(configs whose Q is e4m3 take the bf16 values it was made from) and quantised inside the
+call to e4m3 under one per-tensor scale (amax / 448).
 
 --op sparse times paged_gqa_sparse_attn on the sparse prefill workload (8192 new tokens on
 a 32768-token context, 2051 selected positions per (token, kv head), heads of --sparse-tp):
@@ -207,12 +208,21 @@ def traffic_for(kernel_kind: str, workload: str):
 
 # ------------------------------------------------------------------------ ours --
 
+def attn_spec(args) -> wl.CaseSpec:
+    """The config's workload; for the quantising call its q is given in bf16 (the call
+    makes the e4m3 q itself)."""
+    spec = wl.config_spec(args.config)
+    if args.op == "attn_quant_q" and spec.q_dtype != "bf16":
+        spec = dataclasses.replace(spec, q_dtype="bf16")
+    return spec
+
+
 def run_ours(args, rank, world, local):
     import paged_gqa_gb300 as pg
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pg.load()
-    spec = wl.config_spec(args.config)
+    spec = attn_spec(args)
     case = wl.make_case(spec, device=dev, seed=rank)  # each rank: an independent replica
     T, Hq = case.q.shape[0], case.q.shape[1]
     out = torch.empty(T, Hq, wl.HEAD_DIM, dtype=torch.bfloat16, device=dev)
@@ -223,8 +233,6 @@ def run_ours(args, rank, world, local):
         dominant_cls = 1
 
     quant_q = args.op == "attn_quant_q"
-    if quant_q and spec.q_dtype != "bf16":
-        raise SystemExit(f"--op attn_quant_q needs a workload with a bf16 q (config {args.config} has {spec.q_dtype})")
     attn = pg.paged_gqa_attn_quant_q if quant_q else pg.paged_gqa_attn
 
     def call():
@@ -776,7 +784,7 @@ def cpu_baseline(spec, case, target_s, kind, quant_q=False):
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    spec = wl.config_spec(args.config)
+    spec = attn_spec(args)
     kind = workload_kind(spec)
     # structure on the host, values on the GPU if there is one (fast generation), then host copies
     dev = "cuda" if torch.cuda.is_available() else "cpu"
