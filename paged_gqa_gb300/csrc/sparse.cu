@@ -38,9 +38,11 @@ constexpr int kPairs = 2;                 // units per CTA
 constexpr int kSpThreads = kPairs * 64;
 constexpr float kTauSp = 8.f;             // p <= 2^8 between rescales (f16 holds it exactly)
 
-struct PairSmem {
+struct alignas(16) PairSmem {
   float xs[2][2][32][8];  // [step parity][warp][lane]: the warp's partial S fragment (2 n8 tiles)
 };
+// xs is read and written as float4: every pair's copy must start on 16 bytes
+static_assert(sizeof(PairSmem) % 16 == 0, "PairSmem array elements stay 16-byte aligned");
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
