@@ -587,6 +587,10 @@ int paged_gqa_cache_write(const pg_tensor* k_new, const pg_tensor* v_new, const 
     return fail(PG_ERR_INVALID_ARG, "null data pointer");
   if (!(std::isfinite(k_descale) && k_descale > 0.f && std::isfinite(v_descale) && v_descale > 0.f))
     return fail(PG_ERR_INVALID_ARG, "descales must be finite and positive");
+  if (T == 0) {  // nothing to write: no device is touched
+    t_last_error.clear();
+    return PG_OK;
+  }
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");

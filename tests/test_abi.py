@@ -205,3 +205,15 @@ def _sp_call(a, idx):
 def test_sparse_rejects_bad_arguments_before_any_launch(over, idx, code, msg):
     assert _sp_call(_args(**over), idx) == code
     assert msg in pg.paged_gqa_last_error()
+
+
+def test_sparse_empty_batch_is_a_no_op():
+    a = _args(bt=FakeTensor((0, 5), torch.int32), sl=FakeTensor((0,), torch.int32),
+              qsl=FakeTensor((1,), torch.int32), q=FakeTensor((0, 16, 256), torch.bfloat16),
+              out=FakeTensor((0, 16, 256), torch.bfloat16))
+    assert _sp_call(a, FakeTensor((0, 1, 64), torch.int32)) == 0
+
+
+def test_cache_write_without_new_tokens_is_a_no_op():
+    a = _cw_args(kn=FakeTensor((0, 2, 256), torch.bfloat16), vn=FakeTensor((0, 2, 256), torch.bfloat16))
+    assert _cw_call(a) == 0
