@@ -99,7 +99,10 @@ typedef enum {
  *   query_start_loc [num_seqs + 1]      int32, [0] == 0, non-decreasing, [num_seqs] == T
  *   k_descale, v_descale                per-tensor dequant scales (pass 1 for bf16)
  *   softmax_scale                       multiplies q . k (usually 1/16 for hd 256)
- *   out             [T, Hq, 256]        bf16, written for every (token, head)
+ *   out             [T, Hq, 256]        bf16, written for every (token, head); its
+ *                                        (token, head) rows must not overlap (strides
+ *                                        positive and each at least the span of the
+ *                                        smaller ones, else PG_ERR_INVALID_ARG)
  *   stream                              CUDA stream the work is ordered on
  *
  * Uses a library-owned workspace per device that grows on first need
@@ -197,7 +200,9 @@ int paged_gqa_sparse_attn(const pg_tensor* q, const pg_tensor* k_cache, const pg
  *                                        head_dim contiguous, base and strides multiples
  *                                        of 16 bytes
  *   k_cache, v_cache [NB, P, Hkv, 256]  e4m3, written in place (same layout rules as the
- *                                        call's caches)
+ *                                        call's caches; in addition their (page, slot,
+ *                                        head) rows must not overlap, else
+ *                                        PG_ERR_INVALID_ARG)
  *   block_table, seq_lens, query_start_loc  as in paged_gqa_attn: sequence s's q_len =
  *                                        qsl[s+1] - qsl[s] new tokens take positions
  *                                        seq_lens[s] - q_len .. seq_lens[s] - 1
@@ -205,7 +210,10 @@ int paged_gqa_sparse_attn(const pg_tensor* q, const pg_tensor* k_cache, const pg
  *                                        (finite, > 0)
  *
  * Token t of sequence s lands in page block_table[s][pos / P], slot pos % P, as the e4m3
- * codes of value / descale (computed in fp32, clamped to +-448, rounded to nearest even).
+ * codes of value * inv, where inv = 1 / descale rounded to fp32 once per call and the
+ * product is taken in fp32 (then clamped to +-448, rounded to nearest even). For a
+ * descale that is not a power of two this product can round to a different code than
+ * an fp32 division value / descale would, at an e4m3 tie.
  * Nothing else in the caches changes. Host-side argument errors return a status before any
  * launch; a position or page id out of range is flagged in the device error word
  * (PG_ERR_DEVICE_BOUNDS via paged_gqa_check_device_errors) and that row is skipped.
@@ -219,7 +227,10 @@ int paged_gqa_cache_write(const pg_tensor* k_new, const pg_tensor* v_new, const 
 /*
  * Workspace bytes for a call with these host-known sizes on `device`
  * (num_seqs, total query tokens T, heads, page size, block-table width W).
- * Returns 0 on invalid sizes.
+ * Returns 0 on invalid sizes. The size depends only on num_seqs, T, the head counts and
+ * the device's SM count; page_size and max_blocks_per_seq (which bound every sequence's
+ * length, L <= W * P) are accepted so that the signature stays valid if a later kernel
+ * sizes anything by the longest sequence, and are otherwise unused.
  */
 size_t paged_gqa_workspace_size(int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
                                 int page_size, int max_blocks_per_seq, int device);

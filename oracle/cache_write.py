@@ -8,14 +8,16 @@ cache the attention reads; "Optimize Qwen3.5 MTP unified attention on gfx950" an
 FMHA for prefix-hit prefill" read a cache that this step fills): for sequence s with
 q_len new tokens and total length L (seq_lens, which already counts the new tokens), new
 token t sits at position L - q_len + t, i.e. in page block_table[s][pos // P], slot
-pos % P, and every head's 256 values are stored as e4m3 codes of value / descale (the
-per-tensor descale the attention path multiplies back).
+pos % P, and every head's 256 values are stored as e4m3 codes of value * inv, with inv =
+1 / descale rounded to float32 first (the per-tensor descale the attention path
+multiplies back).
 
 e4m3 (OCP E4M3FN) from its definition: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits;
 exponent field 0 holds subnormals m * 2^-9; the code 0x7F/0xFF is NaN; the largest finite
 value is 448. Encoding clamps to +-448 first, then rounds to the nearest representable
-value, ties to the even mantissa. The division value / descale is taken in float32, as the
-kernel takes it (the rounding that decides a code is taken in the kernel's precision).
+value, ties to the even mantissa. The product value * inv is taken in float32, as the
+kernel takes it (the rounding that decides a code is taken in the kernel's precision); it
+is not the division value / descale, which can round to the other code at an e4m3 tie.
 
 Parity status: pinned (tests/test_cache_write_oracle.py: every finite code round-trips,
 agreement with torch.float8_e4m3fn wherever that cast does not overflow, explicit ties and

@@ -14,6 +14,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <utility>
 
 #include "../../include/paged_gqa.h"
 #include "common.cuh"
@@ -49,6 +50,33 @@ int cuda_fail(cudaError_t e, const char* what) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Whether the rows of a written tensor are pairwise disjoint: dims 0 .. nd-1 index rows of
+// kHeadDim contiguous elements. Sufficient test: taken in increasing stride order, every
+// dim of extent > 1 must step past everything the smaller dims span (no zero, negative or
+// interleaved strides), so no two (index tuples) write the same element.
+bool rows_disjoint(const pg_tensor* t, int nd) {
+  long long ext[4], str[4];
+  int n = 0;
+  for (int i = 0; i < nd; ++i) {
+    if (t->shape[i] <= 1) continue;
+    if (t->stride[i] <= 0) return false;
+    ext[n] = t->shape[i];
+    str[n] = t->stride[i];
+    ++n;
+  }
+  for (int i = 1; i < n; ++i)  // insertion sort by stride
+    for (int j = i; j > 0 && str[j] < str[j - 1]; --j) {
+      std::swap(str[j], str[j - 1]);
+      std::swap(ext[j], ext[j - 1]);
+    }
+  long long span = kHeadDim;  // elements covered by one index of the dims taken so far
+  for (int i = 0; i < n; ++i) {
+    if (str[i] < span) return false;
+    span = (ext[i] - 1) * str[i] + span;
+  }
+  return true;
+}
 
 constexpr int kMaxDevices = 64;
 
@@ -212,6 +240,8 @@ int validate(const pg_tensor* q, const pg_tensor* k, const pg_tensor* v, const p
   if (W > 1 && bt->stride[1] != 1) return fail(PG_ERR_INVALID_ARG, "block_table rows must be contiguous");
   if ((S > 0 && sl->stride[0] != 1) || qsl->stride[0] != 1)
     return fail(PG_ERR_INVALID_ARG, "seq_lens and query_start_loc must be contiguous");
+  if (!rows_disjoint(out, 2))
+    return fail(PG_ERR_INVALID_ARG, "out strides make (token, head) rows overlap");
   const int qesz = q->dtype == PG_E4M3 ? 1 : 2, kesz = k->dtype == PG_E4M3 ? 1 : 2;
   if (!aligned16(q->data) || !aligned16(k->data) || !aligned16(v->data) || !aligned16(out->data))
     return fail(PG_ERR_INVALID_ARG, "q, caches and out must be 16-byte aligned");
@@ -582,6 +612,8 @@ int paged_gqa_cache_write(const pg_tensor* k_new, const pg_tensor* v_new, const 
   for (int i = 0; i < 3; ++i)
     if (k_cache->stride[i] % 16 || v_cache->stride[i] % 16)
       return fail(PG_ERR_INVALID_ARG, "cache strides must be multiples of 16 bytes");
+  if (!rows_disjoint(k_cache, 3) || !rows_disjoint(v_cache, 3))
+    return fail(PG_ERR_INVALID_ARG, "cache strides make (page, slot, head) rows overlap");
   if ((T > 0 && (!k_new->data || !v_new->data)) || (NB > 0 && (!k_cache->data || !v_cache->data)) ||
       !query_start_loc->data || (S > 0 && (!seq_lens->data || (W > 0 && !block_table->data))))
     return fail(PG_ERR_INVALID_ARG, "null data pointer");

@@ -5,8 +5,9 @@
 // gfx950" and "asm FP8 FMHA for prefix-hit prefill" read an FP8 cache that this fills):
 // sequence s's q_len new tokens take positions L - q_len .. L - 1 (seq_lens counts them),
 // position pos lands in page block_table[s][pos / P] at slot pos % P, and each of the 256
-// values of a (token, kv head) row is stored as the e4m3 code of value / descale (clamped
-// to +-448, round to nearest even), which the attention multiplies back.
+// values of a (token, kv head) row is stored as the e4m3 code of value * inv, where inv =
+// 1 / descale rounded to float32 on the host and the product is taken in float32 (then
+// clamped to +-448, round to nearest even); the attention multiplies the descale back.
 //
 // HBM-bound: a (token, kv head) row per warp step, 8 values per lane (16-byte bf16 loads,
 // 8-byte e4m3 stores). Bytes per row: 2 x 512 read + 2 x 256 written.

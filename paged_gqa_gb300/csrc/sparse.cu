@@ -4,7 +4,11 @@
 //
 // The tile of one unit (token t, kv head h, up to 16 of its query heads) has M = 16 rows,
 // too few for a tcgen05 tile: the products run on warp-level mma.sync m16n8k16 (f16 in,
-// fp32 accumulate). e4m3 K/V convert to f16 exactly; bf16 Q is converted to f16 once.
+// fp32 accumulate). e4m3 K/V convert to f16 exactly; bf16 Q is converted to f16 once,
+// after scaling the unit's Q by a power of two 2^sig that puts its largest |q| in
+// [2^14, 2^15): every bf16 value within 2^-24 of that maximum is then exact in f16 (bf16
+// values beyond f16's range, or below its normal range, included), and 2^-sig goes into
+// the score scale.
 //
 // Work split: a pair of warps per unit; warp w owns head dims [128w, 128w + 128). Per step
 // of 16 listed keys each warp computes the partial S of all 16 keys over its d-half (two
@@ -40,6 +44,7 @@ constexpr float kTauSp = 8.f;             // p <= 2^8 between rescales (f16 hold
 
 struct alignas(16) PairSmem {
   float xs[2][2][32][8];  // [step parity][warp][lane]: the warp's partial S fragment (2 n8 tiles)
+  float qmax[4];          // [warp]: max |q| over the warp's d-half of the unit's rows
 };
 // xs is read and written as float4: every pair's copy must start on 16 bytes
 static_assert(sizeof(PairSmem) % 16 == 0, "PairSmem array elements stay 16-byte aligned");
@@ -67,9 +72,14 @@ __device__ __forceinline__ uint32_t byte_pair_f16x2(uint32_t a, uint32_t b, uint
   return e4m3x2_f16x2(r);
 }
 
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+// Two bf16 values times 2^sig (`scale`) -> f16x2.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, float scale) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16) * scale, __uint_as_float(w & 0xffff0000u) * scale);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float bf16x2_absmax(uint32_t w) {
+  return fmaxf(fabsf(__uint_as_float(w << 16)), fabsf(__uint_as_float(w & 0xffff0000u)));
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
@@ -116,28 +126,49 @@ __global__ void __launch_bounds__(kSpThreads, 3) sparse_attn_kernel(SparseArgs a
   // k-step kk (0..7) uses d = 128w + 16 (4 (kk >> 2) + tig) + 4 (kk & 3) .. +3, i.e. of the
   // 16-d chunks tig and 4 + tig of the half, elements 4 (kk & 3) .. +3.
   uint32_t qf[8][4];  // {row g pair 0, row g+8 pair 0, row g pair 1, row g+8 pair 1}
+  uint4 raw[2][4];    // [half]: chunk tig (raw[.][0..1]) and chunk 4 + tig (raw[.][2..3]), bf16
+  float qmax = 0.f;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int r = g + 8 * half;
-    uint4 raw[4];  // chunk tig (raw[0..1]) and chunk 4 + tig (raw[2..3]) of the half, bf16
     if (unit_ok && r < rows) {
       const uint16_t* row = a.q + (long long)t * a.q_st + (long long)(head0 + r) * a.q_sh + 128 * w;
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const uint4* src = reinterpret_cast<const uint4*>(row + 16 * (4 * i + tig));
-        raw[2 * i] = __ldg(src);
-        raw[2 * i + 1] = __ldg(src + 1);
+        raw[half][2 * i] = __ldg(src);
+        raw[half][2 * i + 1] = __ldg(src + 1);
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) raw[i] = make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < 4; ++i) raw[half][i] = make_uint4(0, 0, 0, 0);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) qmax = fmaxf(qmax, bf16x2_absmax(word_of(raw[half][i], k)));
+  }
+  // the unit's max |q| (both warps of the pair), then 2^sig with 2^sig * max in [2^14, 2^15)
+  qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
+  qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
+  qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 4));
+  qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 8));
+  qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 16));
+  if (lane == 0) ps.qmax[w] = qmax;
+  pair_sync(pair);
+  qmax = fmaxf(ps.qmax[0], ps.qmax[1]);
+  int sig = 0;
+  if (qmax > 0.f && qmax <= 3.0e38f) sig = 14 - ((int)((__float_as_uint(qmax) >> 23) & 0xff) - 127);
+  sig = max(-120, min(120, sig));
+  const float qscale = ldexpf(1.f, sig);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const int e0 = 4 * (kk & 3);
-      const uint4& c = raw[2 * (kk >> 2) + (e0 >> 3)];
-      qf[kk][half] = bf16x2_to_f16x2(word_of(c, (e0 & 7) >> 1));
-      qf[kk][2 + half] = bf16x2_to_f16x2(word_of(c, ((e0 & 7) >> 1) + 1));
+      const uint4& c = raw[half][2 * (kk >> 2) + (e0 >> 3)];
+      qf[kk][half] = bf16x2_to_f16x2(word_of(c, (e0 & 7) >> 1), qscale);
+      qf[kk][2 + half] = bf16x2_to_f16x2(word_of(c, ((e0 & 7) >> 1) + 1), qscale);
     }
   }
 
@@ -146,7 +177,7 @@ __global__ void __launch_bounds__(kSpThreads, 3) sparse_attn_kernel(SparseArgs a
   for (int m = 0; m < 16; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
   float m_ref[2] = {-INFINITY, -INFINITY};  // rows g, g+8 (the same in both warps)
   float l_row[2] = {0.f, 0.f};             // this thread's keys' share of the row sums
-  const float c = a.score_scale_log2;
+  const float c = a.score_scale_log2 * ldexpf(1.f, -sig);  // scores of the unscaled q
 
   const int32_t* list = a.idx + (long long)t * a.idx_st + (long long)kvh * a.idx_sh;
   const int K = unit_ok ? a.K : 0;

@@ -90,6 +90,11 @@ def _call(a, scale=1 / 16):
           v=FakeTensor((10, 16, 1, 256), torch.uint8)), -1, "16 bytes"),
     (dict(sl=FakeTensor((2,), torch.float32)), -1, "int32"),
     (dict(out=FakeTensor((9, 16, 256), torch.bfloat16)), -1, "out shape"),
+    # out rows that overlap: a broadcast token axis, heads 128 elements apart, a head axis
+    # stepping inside the token axis' span
+    (dict(out=FakeTensor((8, 16, 256), torch.bfloat16, stride=[0, 256, 1])), -1, "overlap"),
+    (dict(out=FakeTensor((8, 16, 256), torch.bfloat16, stride=[4096, 128, 1])), -1, "overlap"),
+    (dict(out=FakeTensor((8, 16, 256), torch.bfloat16, stride=[256, 1024, 1])), -1, "overlap"),
 ])
 def test_invalid_arguments_are_rejected_on_host(over, code, msg):
     st = _call(_args(**over))
@@ -152,6 +157,8 @@ def _cw_call(a, kd=1.0, vd=1.0):
      "head_dim"),
     (dict(kn=FakeTensor((8, 2, 256), torch.bfloat16, stride=[516, 258, 1])), (1.0, 1.0), -1, "16 bytes"),
     (dict(qsl=FakeTensor((2,), torch.int32)), (1.0, 1.0), -1, "query_start_loc"),
+    (dict(kc=FakeTensor((10, 16, 2, 256), torch.uint8, stride=[8192, 0, 256, 1])), (1.0, 1.0), -1, "overlap"),
+    (dict(vc=FakeTensor((10, 16, 2, 256), torch.uint8, stride=[4096, 512, 128, 1])), (1.0, 1.0), -1, "overlap"),
     ({}, (0.0, 1.0), -1, "positive"),
     ({}, (1.0, float("nan")), -1, "positive"),
 ])

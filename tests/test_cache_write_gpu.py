@@ -80,3 +80,24 @@ def test_bad_page_is_flagged_and_skipped_without_trapping():
                               kc0.cpu().numpy(), case.block_table[1:].cpu().numpy(), case.seq_lens[1:].cpu().numpy(),
                               (case.query_start_loc[1:] - 2).cpu().numpy(), 1.0, 1.0)
     assert (case.k_cache.cpu().numpy() == ref_k).all()
+
+
+def test_tie_input_takes_the_code_of_the_product():
+    """descale 1.7: every positive bf16 value up to 380 written once (and its negation); the inputs where
+    value / descale and value * fl32(1 / descale) round to different e4m3 codes must take
+    the product's code (the oracle's reading), as every other input must match byte for byte."""
+    bits = (torch.arange(1, 0x43BF, dtype=torch.int32) << 16).view(torch.float32)  # 2^-133 .. 380
+    vals = bits.to(torch.bfloat16)
+    n = (vals.numel() + 255) // 256
+    flat = torch.zeros(n * 256, dtype=torch.bfloat16)
+    flat[: vals.numel()] = vals
+    spec = wl.CaseSpec("ties", [(n, n + 5)], 4, 1, 16)
+    case = wl.make_case(spec, device="cuda", seed=63)
+    kn = flat.view(n, 1, 256).cuda()
+    vn = (-flat).view(n, 1, 256).cuda()
+    kc0, vc0 = case.k_cache.clone(), case.v_cache.clone()
+    pg.paged_gqa_cache_write(kn, vn, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                             case.query_start_loc, 1.7, 1.7)
+    assert pg.paged_gqa_check_device_errors() == 0, pg.paged_gqa_last_error()
+    ref_k, ref_v = _oracle(case, kn, vn, kc0, vc0, 1.7, 1.7)
+    assert (case.k_cache.cpu().numpy() == ref_k).all() and (case.v_cache.cpu().numpy() == ref_v).all()

@@ -71,3 +71,31 @@ def test_scatter_puts_new_tokens_at_the_end_of_each_sequence():
             assert (vc[page, slot] == cw.e4m3_encode(vn[qsl[s] + t] * np.float32(0.5))).all()
     assert (kc[~written] == kc0[~written]).all() and (vc[~written] == vc0[~written]).all()
     assert written.sum() == T
+
+
+def _bf16_values():
+    """Every finite non-negative bf16 value, as float32."""
+    return (np.arange(0, 0x7F80, dtype=np.uint32) << 16).view(np.float32)
+
+
+def test_code_is_the_product_with_the_fp32_reciprocal_not_the_division():
+    # The reading of the write: code = e4m3(value * fl32(1 / descale)), the product in fp32.
+    # For a descale that is not a power of two, a few bf16 inputs sit where value / descale
+    # and value * fl32(1 / descale) fall on the two sides of an e4m3 tie; the write must
+    # take the product's code there.
+    x = _bf16_values()
+    d = np.float32(1.7)
+    inv = np.float32(1.0) / d
+    with np.errstate(over="ignore"):
+        by_div, by_mul = cw.e4m3_encode(x / d), cw.e4m3_encode(x * inv)
+    differ = np.nonzero(by_div != by_mul)[0]
+    assert len(differ) >= 1
+    v = float(x[differ[0]])
+    P, Hkv = 16, 1
+    kn = np.full((1, Hkv, 256), v, np.float32)
+    kc0 = np.zeros((2, P, Hkv, 256), np.uint8)
+    bt = np.array([[1]], np.int32)
+    kc, vc = cw.cache_write(kn, -kn, kc0, kc0, bt, np.array([5], np.int32), np.array([0, 1], np.int32),
+                            float(d), float(d))
+    assert (kc[1, 4] == by_mul[differ[0]]).all() and (kc[1, 4] != by_div[differ[0]]).all()
+    assert (vc[1, 4] == (by_mul[differ[0]] | 0x80)).all()

@@ -124,3 +124,22 @@ def test_sparse_prefill_workload_sampled_rows():
                       torch.arange((spec.total_q - 1) * Hq, spec.total_q * Hq)]).numpy().astype(np.int64)
     ref = _oracle(case, idx, rows=rows)
     gu.compare(got[torch.from_numpy(rows).cuda()], ref, "sparse prefill TP1 sampled rows")
+
+
+@pytest.mark.parametrize("qscale", [1e5, 1e-6])
+def test_q_beyond_the_f16_range(qscale):
+    """bf16 q far outside f16's normal range (|q| ~ 1e5 overflows f16, ~1e-6 is subnormal
+    there), with softmax_scale scaled the other way so that the scores are those of N(0, 1)
+    inputs: the result must still match the oracle on the same bf16 q."""
+    import dataclasses
+    gen = torch.Generator().manual_seed(96)
+    spec = wl.random_small_spec(gen, group=12, num_kv_heads=1, page_size=16, q_lens=[5, 2], max_ctx=300,
+                                kv_dtype="e4m3", q_dtype="bf16")
+    spec = dataclasses.replace(spec, softmax_scale=spec.softmax_scale / qscale)
+    case = wl.make_case(spec, device="cuda", seed=96, poison=True)
+    q = (case.q.float() * qscale).to(torch.bfloat16)
+    assert (q.float().abs().max() > 65504) if qscale > 1 else (q.float().abs().max() < 6.1e-5)
+    case = wl.Case(spec, q, case.k_cache, case.v_cache, case.block_table, case.seq_lens, case.query_start_loc,
+                   case.q_descale, case.k_descale, case.v_descale, spec.softmax_scale)
+    idx = _random_lists(case, 60, 96)
+    gu.compare(_run(case, idx), _oracle(case, idx), f"sparse, q x {qscale:g}")

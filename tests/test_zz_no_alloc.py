@@ -67,16 +67,19 @@ def test_noalloc_matches_regular_entry_point_on_calls_in_a_row():
 
 def test_noalloc_rejects_calls_beyond_its_scratch():
     import paged_gqa_gb300 as pg
-    n = 1 << 20  # a million one-token sequences need more than the 64 MiB scratch
-    need = pg.paged_gqa_workspace_size(n, n, 16, 1, 16, 1, torch.cuda.current_device())
+    # a million sequences (one query token in all, the rest with q_len 0) on two kv heads:
+    # their verify blocks alone need more than the 64 MiB scratch
+    n = 1 << 20
+    need = pg.paged_gqa_workspace_size(n, 1, 32, 2, 16, 1, torch.cuda.current_device())
     assert need > (64 << 20)
-    q = torch.zeros(1, 16, 256, dtype=torch.bfloat16, device="cuda").expand(n, 16, 256)
-    kv = torch.zeros(4, 16, 1, 256, dtype=torch.uint8, device="cuda")
-    case = wl.Case(wl.CaseSpec("big", [(1, 1)], 16, 1, 16), q, kv, kv,
+    q = torch.zeros(1, 32, 256, dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros(4, 16, 2, 256, dtype=torch.uint8, device="cuda")
+    qsl = torch.ones(n + 1, dtype=torch.int32, device="cuda")
+    qsl[0] = 0
+    case = wl.Case(wl.CaseSpec("big", [(1, 1)], 32, 2, 16), q, kv, kv,
                    torch.zeros(n, 1, dtype=torch.int32, device="cuda"),
-                   torch.ones(n, dtype=torch.int32, device="cuda"),
-                   torch.arange(n + 1, dtype=torch.int32, device="cuda"), 1.0, 1.0, 1.0, 1.0 / 16)
-    out = torch.zeros(1, 16, 256, dtype=torch.bfloat16, device="cuda").expand(n, 16, 256)
+                   torch.ones(n, dtype=torch.int32, device="cuda"), qsl, 1.0, 1.0, 1.0, 1.0 / 16)
+    out = torch.zeros(1, 32, 256, dtype=torch.bfloat16, device="cuda")
     st = _call_noalloc(case, out)
     assert st == -6
     assert "workspace too small" in pg.paged_gqa_last_error()
