@@ -70,6 +70,10 @@ def parse():
     ap.add_argument("--write-case", default="config", choices=["config", "chunks"],
                     help="cache_write: the config's new tokens, or 32 fresh 4096-token chunks (profiling size)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--extra-cpu-seconds", type=float, default=3.0,
+                    help="target CPU time of the oracle sample of each extra workload")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="time only --config (by default the MTP verify line also times workloads 1, 3, 4, 5)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -217,35 +221,14 @@ def attn_spec(args) -> wl.CaseSpec:
     return spec
 
 
-def run_ours(args, rank, world, local):
-    import paged_gqa_gb300 as pg
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    pg.load()
-    spec = attn_spec(args)
-    case = wl.make_case(spec, device=dev, seed=rank)  # each rank: an independent replica
-    T, Hq = case.q.shape[0], case.q.shape[1]
-    out = torch.empty(T, Hq, wl.HEAD_DIM, dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    kind = workload_kind(spec)
-    dominant_cls = 0 if kind == "hbm" else 1
-    if args.config == 5:
-        dominant_cls = 1
-
-    quant_q = args.op == "attn_quant_q"
-    attn = pg.paged_gqa_attn_quant_q if quant_q else pg.paged_gqa_attn
-
-    def call():
-        attn(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
-             case.query_start_loc, case.k_descale, case.v_descale, case.softmax_scale, out)
-
-    for _ in range(max(3, args.warmup)):
+def _time_attn(pg, call, flush, K, warmup, dominant_cls, local, world):
+    """Per-call CUDA events over K calls (an L2 flush before each, outside the events),
+    then a second pass with the library's events around the dominant kernel. Returns
+    (call_ms list, kernel_ms list, clocks, wall_s)."""
+    for _ in range(max(3, warmup)):
         call()
     torch.cuda.synchronize()
     assert pg.paged_gqa_check_device_errors() == 0, pg.paged_gqa_last_error()
-    plan = pg.paged_gqa_last_plan()
-
-    K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(local)
@@ -273,9 +256,99 @@ def run_ours(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    call_ms = [a.elapsed_time(b) for a, b in ev]
-    kern_ms = [a.elapsed_time(b) for a, b in kev]
-    step_ms = sum(call_ms) / K
+    assert pg.paged_gqa_check_device_errors() == 0, pg.paged_gqa_last_error()
+    return [a.elapsed_time(b) for a, b in ev], [a.elapsed_time(b) for a, b in kev], clocks, wall
+
+
+def _roofline(spec, kind, kern_ms_mean, kernel_kind):
+    hbm, bf16, _, peak_src = load_peaks()
+    if kind == "hbm":
+        units, peak, peak_unit = spec.kv_bytes / 1e9, hbm, "GB/s"
+        src = f"{peak_src} (hbm_gbs)"
+    else:
+        units, peak, peak_unit = spec.flops / 1e12, 2 * bf16, "TFLOP/s"  # FP8 dense = 2 x bf16 (nominal ratio)
+        src = f"{peak_src} (2 x bf16_tflops burst)"
+    achieved = units / (kern_ms_mean / 1e3)
+    return {"bound": kind, "achieved": round(achieved, 2), "peak": peak, "unit": peak_unit,
+            "frac": round(achieved / peak, 4), "peak_source": src, "kernel": kernel_kind,
+            "kernel_us": round(kern_ms_mean * 1e3, 2), "traffic": traffic_for(kernel_kind, spec.name)}
+
+
+def _dominant(spec, config_index):
+    kind = workload_kind(spec)
+    cls = 0 if kind == "hbm" else 1
+    if config_index == 5:
+        cls = 1  # the mixed batch: prefill blocks hold nearly all of the work
+    return kind, cls
+
+
+def _kernel_kind(plan, cls, kind):
+    """Name of the class-`cls` kernel the last call ran (its traffic.json key prefix)."""
+    return ("verify" if cls == 0 else "prefill") if plan["path_bits"] & (2 << cls) else "portable"
+
+
+def extra_config(pg, args, idx, dev, flush, local, world, quant_q):
+    """One more workload timed in the same run: median/mean us per call, the dominant
+    kernel's roofline, clocks and a short oracle sample."""
+    spec = dataclasses.replace(wl.config_spec(idx), q_dtype="bf16") if quant_q else wl.config_spec(idx)
+    if quant_q and spec.kv_dtype != "e4m3":
+        return None
+    case = wl.make_case(spec, device=dev, seed=0)
+    T, Hq = case.q.shape[0], case.q.shape[1]
+    out = torch.empty(T, Hq, wl.HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    attn = pg.paged_gqa_attn_quant_q if quant_q else pg.paged_gqa_attn
+
+    def call():
+        attn(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+             case.query_start_loc, case.k_descale, case.v_descale, case.softmax_scale, out)
+
+    kind, cls = _dominant(spec, idx)
+    K = max(5, min(args.steps, 20))
+    call_ms, kern_ms, clocks, _ = _time_attn(pg, call, flush, K, args.warmup, cls, local, world)
+    plan = pg.paged_gqa_last_plan()
+    med, mean = statistics.median(call_ms), sum(call_ms) / K
+    per = spec.kv_bytes / 1e9 if kind == "hbm" else spec.flops / 1e12
+    r = {"workload": spec.name + (":quant_q" if quant_q else ""), "steps": K,
+         "value": round(per / (med / 1e3), 3), "unit": "GB/s" if kind == "hbm" else "TFLOP/s",
+         "us_per_call": round(med * 1e3, 2), "us_per_call_mean": round(mean * 1e3, 2),
+         "kernel_us_median": round(statistics.median(kern_ms) * 1e3, 2),
+         "roofline": _roofline(spec, kind, sum(kern_ms) / K, _kernel_kind(plan, cls, kind)),
+         "path_bits": int(plan["path_bits"]), "clocks": clocks, "kv_bytes": spec.kv_bytes, "flops": spec.flops}
+    if kind == "tensor":
+        # the attainable bound with P.V at f16 precision: half the FLOPs at the FP8 rate and
+        # half at the f16 rate (2/3 of the FP8 peak)
+        r["roofline"]["frac_of_mixed_fp8_f16_bound"] = round(r["roofline"]["frac"] * 1.5, 4)
+    if not args.no_cpu_baseline:
+        r["cpu_baseline"] = cpu_baseline(spec, case, args.extra_cpu_seconds, kind, quant_q)
+    del case, out
+    torch.cuda.empty_cache()
+    return r
+
+
+def run_ours(args, rank, world, local):
+    import paged_gqa_gb300 as pg
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg.load()
+    spec = attn_spec(args)
+    case = wl.make_case(spec, device=dev, seed=rank)  # each rank: an independent replica
+    T, Hq = case.q.shape[0], case.q.shape[1]
+    out = torch.empty(T, Hq, wl.HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    kind, dominant_cls = _dominant(spec, args.config)
+
+    quant_q = args.op == "attn_quant_q"
+    attn = pg.paged_gqa_attn_quant_q if quant_q else pg.paged_gqa_attn
+
+    def call():
+        attn(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+             case.query_start_loc, case.k_descale, case.v_descale, case.softmax_scale, out)
+
+    K = args.steps
+    call_ms, kern_ms, clocks, wall = _time_attn(pg, call, flush, K, args.warmup, dominant_cls, local, world)
+    plan = pg.paged_gqa_last_plan()
+    step_ms = statistics.median(call_ms)
+    step_mean_ms = sum(call_ms) / K
     kern_avg_ms = sum(kern_ms) / K
 
     # e2e: pinned host inputs -> device, call, device -> host result, every step
@@ -304,49 +377,49 @@ def run_ours(args, rank, world, local):
             e2e_step()
             e_ev[i][1].record()
         torch.cuda.synchronize()
-        e2e_ms = sum(a.elapsed_time(b) for a, b in e_ev) / K
+        e2e_ms = statistics.median(a.elapsed_time(b) for a, b in e_ev)
         e2e = (e2e_ms, h2d, d2h)
 
     # reduce over ranks: max time
-    step_ms, kern_avg_ms, e2e_ms = max_over_ranks([step_ms, kern_avg_ms, e2e[0] if e2e else 0.0], world, dev)
+    step_ms, step_mean_ms, kern_avg_ms, e2e_ms = max_over_ranks(
+        [step_ms, step_mean_ms, kern_avg_ms, e2e[0] if e2e else 0.0], world, dev)
     if rank != 0:
         return None
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(spec, case, args.cpu_seconds, kind, quant_q)
+    extras = {}
+    if world == 1 and not args.no_extra_configs and args.config == 2 and args.op in ("attn", "attn_quant_q"):
+        for idx in (1, 3, 4, 5):
+            r = extra_config(pg, args, idx, dev, flush, local, world, quant_q)
+            if r is not None:
+                extras[str(idx)] = r
 
-    hbm, bf16, bf16_sus, peak_src = load_peaks()
-    if kind == "hbm":
-        unit, per_step = "GB/s", spec.kv_bytes / 1e9
-        kern_units = spec.kv_bytes / 1e9
-        peak, peak_unit = hbm, "GB/s"
-        traffic_kind = "verify"
-    else:
-        unit, per_step = "TFLOP/s", spec.flops / 1e12
-        kern_units = spec.flops / 1e12
-        peak, peak_unit = 2 * bf16, "TFLOP/s"  # FP8 dense = 2 x measured bf16 (nominal ratio)
-        traffic_kind = "prefill"
+    per_step = spec.kv_bytes / 1e9 if kind == "hbm" else spec.flops / 1e12
+    unit = "GB/s" if kind == "hbm" else "TFLOP/s"
     value = whole_job_value(per_step, world, step_ms)
-    achieved = kern_units / (kern_avg_ms / 1e3)
-    used = plan["path_bits"]
-    kernel_kind = traffic_kind if used & (2 << dominant_cls) else "portable"
+    kernel_kind = _kernel_kind(plan, dominant_cls, kind)
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "us_per_call": round(step_ms * 1e3, 2),
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "ms_per_step_mean": round(step_mean_ms, 5),
+        "us_per_call": round(step_ms * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if kernel_kind != "portable" else "tf32",
         "data": "synthetic (seeded N(0,1), FP8 per-tensor amax/448)",
         "config": config_dict(spec, args.config, world, "flushed: 512 MiB memset between timed calls", quant_q),
-        "roofline": {"bound": kind, "achieved": round(achieved, 2), "peak": peak, "unit": peak_unit,
-                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} ({'hbm_gbs' if kind == 'hbm' else '2 x bf16_tflops burst'})",
-                     "kernel": kernel_kind, "kernel_us": round(kern_avg_ms * 1e3, 2),
-                     "traffic": traffic_for(kernel_kind, spec.name)},
+        "roofline": _roofline(spec, kind, kern_avg_ms, kernel_kind),
         "gpu_launches": int(plan["kernels_launched"]) * K,
         "clocks": clocks,
         "wall_s": round(wall, 3),
+        "stat": "value and ms_per_step from the median call; roofline.achieved from the mean kernel time",
     }
     if e2e:
         res["e2e"] = {"value": round(per_step * world / (e2e_ms / 1e3), 3), "unit": unit,
                       "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2],
                       "note": "per step: q, block_table, seq_lens, query_start_loc H2D from pinned memory; out D2H; KV cache resident"}
-    if world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(spec, case, args.cpu_seconds, kind, quant_q)
+    if cpu is not None:
+        res["cpu_baseline"] = cpu
+    if extras:
+        res["configs"] = extras
     return res
 
 

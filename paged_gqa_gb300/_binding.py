@@ -3,6 +3,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import struct
 import threading
 from typing import Optional
 
@@ -37,6 +38,20 @@ class PgTensor(ctypes.Structure):
 _lock = threading.Lock()
 _lib = None
 
+# Descriptors are packed into a per-thread array of pg_tensor and passed by address: one
+# struct.pack_into per tensor instead of a ctypes Structure built field by field.
+_DESC_FMT = struct.Struct("=Qii4q4q")
+assert ctypes.sizeof(PgTensor) == _DESC_FMT.size == 80
+_tls = threading.local()
+
+
+def _desc_buf():
+    b = getattr(_tls, "buf", None)
+    if b is None:
+        arr = (PgTensor * 10)()
+        b = _tls.buf = (arr, ctypes.addressof(arr), memoryview(arr).cast("B"))
+    return b
+
 
 def lib_path() -> str:
     return _build.LIB
@@ -45,6 +60,8 @@ def lib_path() -> str:
 def load(build_if_missing: bool = True):
     """Load the library (building it first if it is missing or stale)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if build_if_missing:
@@ -52,7 +69,7 @@ def load(build_if_missing: bool = True):
             if not os.path.exists(_build.LIB):
                 raise RuntimeError(f"libpaged_gqa.so not found at {_build.LIB}; run paged_gqa_gb300.build")
             lib = ctypes.CDLL(_build.LIB)
-            P = ctypes.POINTER(PgTensor)
+            P = ctypes.c_void_p  # descriptors are passed as addresses (see _pack)
             f, c_vp = ctypes.c_float, ctypes.c_void_p
             lib.paged_gqa_attn.argtypes = [P, P, P, P, P, P, f, f, f, P, c_vp]
             lib.paged_gqa_attn.restype = ctypes.c_int
@@ -107,6 +124,26 @@ def _desc(t: Optional[torch.Tensor], dtype: Optional[int] = None) -> PgTensor:
     return d
 
 
+def _pack(*tensors):
+    """Addresses of pg_tensor descriptors of the given tensors, valid until the next call
+    from this thread (the library copies what it needs before it returns)."""
+    arr, base, mv = _desc_buf()
+    pack, dt = _DESC_FMT.pack_into, _DTYPES
+    out = []
+    for i, t in enumerate(tensors):
+        off = 80 * i
+        n = t.dim()
+        if n > 4:
+            raise ValueError("at most 4 dims")
+        sh, st = tuple(t.shape), t.stride()
+        if n < 4:
+            sh = sh + (0,) * (4 - n)
+            st = st + (0,) * (4 - n)
+        pack(mv, off, t.data_ptr() if t.numel() > 0 else 0, dt[t.dtype], n, *sh, *st)
+        out.append(base + off)
+    return out
+
+
 def _stream(stream) -> int:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -125,11 +162,9 @@ def paged_gqa_attn(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, 
                    v_descale: float, softmax_scale: float, out, stream=None) -> None:
     """out[T, Hq, 256] (bf16) = paged GQA attention; see include/paged_gqa.h."""
     lib = load()
-    a = [_desc(q), _desc(k_cache), _desc(v_cache), _desc(block_table), _desc(seq_lens),
-         _desc(query_start_loc)]
-    o = _desc(out)
-    _check(lib.paged_gqa_attn(*[ctypes.byref(x) for x in a], float(k_descale), float(v_descale),
-                              float(softmax_scale), ctypes.byref(o), _stream(stream)))
+    d = _pack(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out)
+    _check(lib.paged_gqa_attn(*d[:6], float(k_descale), float(v_descale), float(softmax_scale), d[6],
+                              _stream(stream)))
 
 
 def paged_gqa_attn_ex(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, q_descale: float,
@@ -137,46 +172,37 @@ def paged_gqa_attn_ex(q, k_cache, v_cache, block_table, seq_lens, query_start_lo
                       stream=None) -> None:
     """Same as paged_gqa_attn with q_descale and a caller-owned workspace tensor."""
     lib = load()
-    a = [_desc(q), _desc(k_cache), _desc(v_cache), _desc(block_table), _desc(seq_lens),
-         _desc(query_start_loc)]
-    o = _desc(out)
+    d = _pack(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out)
     nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     ptr = workspace.data_ptr() if workspace is not None else None
-    _check(lib.paged_gqa_attn_ex(*[ctypes.byref(x) for x in a], float(q_descale), float(k_descale),
-                                 float(v_descale), float(softmax_scale), ctypes.byref(o), ptr, nbytes,
-                                 _stream(stream)))
+    _check(lib.paged_gqa_attn_ex(*d[:6], float(q_descale), float(k_descale), float(v_descale),
+                                 float(softmax_scale), d[6], ptr, nbytes, _stream(stream)))
 
 
 def paged_gqa_attn_quant_q(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, k_descale: float,
                            v_descale: float, softmax_scale: float, out, stream=None) -> None:
     """paged_gqa_attn on a bf16 q quantised inside the call to e4m3 with one per-tensor scale."""
     lib = load()
-    a = [_desc(q), _desc(k_cache), _desc(v_cache), _desc(block_table), _desc(seq_lens),
-         _desc(query_start_loc)]
-    o = _desc(out)
-    _check(lib.paged_gqa_attn_quant_q(*[ctypes.byref(x) for x in a], float(k_descale), float(v_descale),
-                                      float(softmax_scale), ctypes.byref(o), _stream(stream)))
+    d = _pack(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out)
+    _check(lib.paged_gqa_attn_quant_q(*d[:6], float(k_descale), float(v_descale), float(softmax_scale), d[6],
+                                      _stream(stream)))
 
 
 def paged_gqa_sparse_attn(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, indices,
                           k_descale: float, v_descale: float, softmax_scale: float, out, stream=None) -> None:
     """Sparse paged GQA attention: row (t, h) attends the listed positions indices[t, h // G]."""
     lib = load()
-    a = [_desc(q), _desc(k_cache), _desc(v_cache), _desc(block_table), _desc(seq_lens),
-         _desc(query_start_loc), _desc(indices)]
-    o = _desc(out)
-    _check(lib.paged_gqa_sparse_attn(*[ctypes.byref(x) for x in a], float(k_descale), float(v_descale),
-                                     float(softmax_scale), ctypes.byref(o), _stream(stream)))
+    d = _pack(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, indices, out)
+    _check(lib.paged_gqa_sparse_attn(*d[:7], float(k_descale), float(v_descale), float(softmax_scale), d[7],
+                                     _stream(stream)))
 
 
 def paged_gqa_cache_write(k_new, v_new, k_cache, v_cache, block_table, seq_lens, query_start_loc,
                           k_descale: float, v_descale: float, stream=None) -> None:
     """Write the new tokens' K and V (bf16 [T, Hkv, 256]) into the e4m3 paged caches."""
     lib = load()
-    a = [_desc(k_new), _desc(v_new), _desc(k_cache), _desc(v_cache), _desc(block_table), _desc(seq_lens),
-         _desc(query_start_loc)]
-    _check(lib.paged_gqa_cache_write(*[ctypes.byref(x) for x in a], float(k_descale), float(v_descale),
-                                     _stream(stream)))
+    d = _pack(k_new, v_new, k_cache, v_cache, block_table, seq_lens, query_start_loc)
+    _check(lib.paged_gqa_cache_write(*d, float(k_descale), float(v_descale), _stream(stream)))
 
 
 def paged_gqa_workspace_size(num_seqs: int, total_q: int, num_q_heads: int, num_kv_heads: int,

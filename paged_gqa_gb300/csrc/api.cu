@@ -324,13 +324,16 @@ int run(const Validated& val, const pg_tensor* k, const pg_tensor* v, void* ws, 
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   ++launched;
   int used = 0;
+  bool prev_ev = false;  // an event was recorded after the previous class's kernel
   for (int c = 0; c < kNumClasses; ++c) {
     bool done = false;
     cudaEvent_t ev0 = g_ev_start[c].load(), ev1 = g_ev_stop[c].load();
     if (ev0 && (e = cudaEventRecord(ev0, stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     if (fast_ok) {
+      // the prefill-class kernel follows the verify-class one as a programmatic dependent
+      // (when that one is a tcgen05 kernel too and no event sits between them)
       int r = (c == 0) ? launch_verify_tc(p, ptr, cp[c], k, v, ds->sms, stream)
-                       : launch_prefill_tc(p, ptr, cp[c], k, v, ds->sms, stream);
+                       : launch_prefill_tc(p, ptr, cp[c], k, v, ds->sms, stream, (used & 2) && !ev0 && !prev_ev);
       if (r < 0) return fail(PG_ERR_CUDA, "tcgen05 %s launch failed: %s", c == 0 ? "verify" : "prefill",
                              tc_last_error());
       if (r == 1) {
@@ -346,6 +349,7 @@ int run(const Validated& val, const pg_tensor* k, const pg_tensor* v, void* ws, 
     }
     ++launched;
     if (ev1 && (e = cudaEventRecord(ev1, stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    prev_ev = ev1 != nullptr;
   }
   plan_info[0] = cp[0].num_ctas;
   plan_info[1] = cp[1].num_ctas;

@@ -294,7 +294,7 @@ cudaError_t launch_portable(const Problem& p, const Pointers& ptr, const ClassPl
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  cudaError_t e = launch_pdl(portable_attn_kernel, cp.num_ctas, kPThreads, kPSmemBytes, stream, p, ptr, cp);
+  cudaError_t e = launch_pdl(false, portable_attn_kernel, cp.num_ctas, kPThreads, kPSmemBytes, stream, p, ptr, cp);
   return e == cudaSuccess ? cudaGetLastError() : e;
 }
 

@@ -643,7 +643,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 }
 
 int launch_prefill_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp, const pg_tensor* k,
-                      const pg_tensor* v, int sms, cudaStream_t stream) {
+                      const pg_tensor* v, int sms, cudaStream_t stream, bool dependent) {
   (void)sms;
   if (!p.kv_is_fp8) return 0;
   CUtensorMap tk, tv;
@@ -666,7 +666,7 @@ int launch_prefill_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp
     }
     attr_done[dev] |= which;
   }
-  e = launch_pdl(kern, cp.num_ctas, kThreads, bytes, stream, tk, tv, p, ptr, cp);
+  e = launch_pdl(dependent, kern, cp.num_ctas, kThreads, bytes, stream, tk, tv, p, ptr, cp);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     char buf[160];

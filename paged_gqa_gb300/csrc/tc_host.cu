@@ -41,10 +41,73 @@ void set_tc_error(const char* msg) { snprintf(t_tc_err, sizeof t_tc_err, "%s", m
 
 const char* tc_last_error() { return t_tc_err; }
 
+namespace {
+
+// Encoded maps of recent caches. A serving loop passes the same cache tensors on every
+// call, so the map (a host-side encode of ~1-2 us each, two per kernel) is looked up
+// instead of re-encoded. The key is everything the encode reads from the descriptor.
+struct TmapKey {
+  const void* data;
+  int dtype;
+  int64_t shape[4];
+  int64_t stride[3];
+  int P;
+  bool operator==(const TmapKey& o) const {
+    if (data != o.data || dtype != o.dtype || P != o.P) return false;
+    for (int i = 0; i < 4; ++i)
+      if (shape[i] != o.shape[i]) return false;
+    for (int i = 0; i < 3; ++i)
+      if (stride[i] != o.stride[i]) return false;
+    return true;
+  }
+};
+constexpr int kTmapCache = 16;
+struct TmapEntry {
+  TmapKey key;
+  CUtensorMap map;
+  bool used;
+};
+TmapEntry g_tmap_cache[kTmapCache];
+int g_tmap_next = 0;
+std::mutex g_tmap_mu;
+
+bool encode_cache_tmap(CUtensorMap* m, const pg_tensor* t, int P);
+
+}  // namespace
+
+// 4-D map over an e4m3 cache [NB, P, Hkv, 256] (see encode_cache_tmap), from the cache of
+// recent maps when the same tensor view was seen before.
+bool make_cache_tmap(CUtensorMap* m, const pg_tensor* t, int P) {
+  TmapKey k{};
+  k.data = t->data;
+  k.dtype = t->dtype;
+  for (int i = 0; i < 4; ++i) k.shape[i] = t->shape[i];
+  for (int i = 0; i < 3; ++i) k.stride[i] = t->stride[i];
+  k.P = P;
+  {
+    std::lock_guard<std::mutex> lk(g_tmap_mu);
+    for (int i = 0; i < kTmapCache; ++i)
+      if (g_tmap_cache[i].used && g_tmap_cache[i].key == k) {
+        *m = g_tmap_cache[i].map;
+        return true;
+      }
+  }
+  if (!encode_cache_tmap(m, t, P)) return false;
+  std::lock_guard<std::mutex> lk(g_tmap_mu);
+  TmapEntry& e = g_tmap_cache[g_tmap_next];
+  g_tmap_next = (g_tmap_next + 1) % kTmapCache;
+  e.key = k;
+  e.map = *m;
+  e.used = true;
+  return true;
+}
+
+namespace {
+
 // 4-D map over an e4m3 cache [NB, P, Hkv, 256]: box = one d-half (128 B) x 1 head x P rows
 // x 1 page, 128-byte swizzle, so one box lands a page's half-rows in the layout the MMA
 // descriptors expect (8-row atoms of 128 B).
-bool make_cache_tmap(CUtensorMap* m, const pg_tensor* t, int P) {
+bool encode_cache_tmap(CUtensorMap* m, const pg_tensor* t, int P) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     set_tc_error("cuTensorMapEncodeTiled unavailable");
@@ -66,5 +129,7 @@ bool make_cache_tmap(CUtensorMap* m, const pg_tensor* t, int P) {
   }
   return true;
 }
+
+}  // namespace
 
 }  // namespace pgqa

@@ -905,7 +905,7 @@ int launch_verify_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp,
     }
     attr_done[dev] |= which;
   }
-  e = launch_pdl(kern, cp.num_ctas, kVThreads, kSmemBytes, stream, tk, tv, p, ptr, cp);
+  e = launch_pdl(false, kern, cp.num_ctas, kVThreads, kSmemBytes, stream, tk, tv, p, ptr, cp);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     char buf[160];
