@@ -253,6 +253,19 @@ int paged_gqa_check_device_errors(pg_stream_t stream);
 int paged_gqa_set_path(int path);
 
 /*
+ * Failure-path test hook (process-wide; for tests of the error path only). With wait_ns
+ * > 0, every CTA of the tcgen05 attention kernels first waits wait_ns nanoseconds on a
+ * shared-memory barrier that nothing arrives on. That bounded wait runs out, the CTA
+ * records PG_ERR_TIMEOUT in the device error word and takes its abort path (every other
+ * wait gives up at once; each role still waits for its own TMA copies and MMAs, then TMEM
+ * is freed), so the call's output is unspecified and paged_gqa_check_device_errors()
+ * returns PG_ERR_TIMEOUT. Nothing faults, traps or hangs; the context stays usable.
+ * wait_ns = 0 (the default) turns it off. Returns the previous value.
+ * (The pages describe no such hook: it tests this library's bounded waits.)
+ */
+int paged_gqa_set_stall_test(uint32_t wait_ns);
+
+/*
  * Host-side launch summary of the last successful call on this host thread, for
  * tests and the benchmark. out8 receives {verify CTAs, prefill CTAs, kernels
  * launched, path bits (2: tcgen05 verify, 4: tcgen05 prefill, 8: warp-MMA verify,

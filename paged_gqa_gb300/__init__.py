@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401
     paged_gqa_last_plan,
     paged_gqa_set_kernel_events,
     paged_gqa_set_path,
+    paged_gqa_set_stall_test,
     paged_gqa_version,
     paged_gqa_workspace_size,
     exported_symbols,

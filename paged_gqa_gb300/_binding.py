@@ -20,7 +20,7 @@ EXPORTED = ("paged_gqa_attn", "paged_gqa_attn_ex", "paged_gqa_attn_noalloc", "pa
             "paged_gqa_sparse_attn", "paged_gqa_cache_write",
             "paged_gqa_workspace_size",
             "paged_gqa_last_error",
-            "paged_gqa_check_device_errors", "paged_gqa_set_path", "paged_gqa_last_plan",
+            "paged_gqa_check_device_errors", "paged_gqa_set_path", "paged_gqa_set_stall_test", "paged_gqa_last_plan",
             "paged_gqa_set_kernel_events", "paged_gqa_version")
 
 
@@ -88,6 +88,8 @@ def load(build_if_missing: bool = True):
             lib.paged_gqa_check_device_errors.restype = ctypes.c_int
             lib.paged_gqa_set_path.argtypes = [ctypes.c_int]
             lib.paged_gqa_set_path.restype = ctypes.c_int
+            lib.paged_gqa_set_stall_test.argtypes = [ctypes.c_uint32]
+            lib.paged_gqa_set_stall_test.restype = ctypes.c_int
             lib.paged_gqa_last_plan.argtypes = [ctypes.POINTER(ctypes.c_int64)]
             lib.paged_gqa_last_plan.restype = ctypes.c_int
             lib.paged_gqa_version.restype = ctypes.c_int
@@ -225,6 +227,12 @@ def paged_gqa_set_path(path: int) -> int:
     if r < 0:
         _check(r)
     return r
+
+
+def paged_gqa_set_stall_test(wait_ns: int) -> int:
+    """Failure-path test hook: tcgen05 CTAs first wait wait_ns on a barrier nothing
+    arrives on (0 turns it off). Returns the previous value."""
+    return int(load().paged_gqa_set_stall_test(int(wait_ns)))
 
 
 def paged_gqa_last_plan() -> dict:

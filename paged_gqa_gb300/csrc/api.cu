@@ -33,6 +33,7 @@ namespace {
 thread_local std::string t_last_error;
 thread_local int64_t t_last_plan[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 std::atomic<int> g_path{0};
+std::atomic<uint32_t> g_stall_test_ns{0};
 std::atomic<cudaEvent_t> g_ev_start[kNumClasses], g_ev_stop[kNumClasses];
 
 int fail(int code, const char* fmt, ...) {
@@ -284,6 +285,7 @@ int validate(const pg_tensor* q, const pg_tensor* k, const pg_tensor* v, const p
   p.bt_stride = W > 0 ? bt->stride[0] : 1;
   p.score_scale_log2 = (float)((double)softmax_scale * (double)q_descale * (double)k_descale * 1.4426950408889634);
   p.out_scale = v_descale;
+  p.stall_test_ns = g_stall_test_ns.load();
   Pointers& ptr = res->ptr;
   ptr.q = q->data;
   ptr.k = k->data;
@@ -558,6 +560,8 @@ int paged_gqa_set_path(int path) {
   if (path < 0 || path > 1) return fail(PG_ERR_INVALID_ARG, "path must be 0 or 1");
   return g_path.exchange(path);
 }
+
+int paged_gqa_set_stall_test(uint32_t wait_ns) { return (int)g_stall_test_ns.exchange(wait_ns); }
 
 int paged_gqa_last_plan(int64_t* out8) {
   if (!out8) return fail(PG_ERR_INVALID_ARG, "null output");

@@ -68,6 +68,10 @@ struct Problem {
   long long bt_stride;
   float score_scale_log2;  // softmax_scale * q_descale * k_descale * log2(e)
   float out_scale;         // v_descale
+  // Failure-path test (0 = off): the softmax warps of every tcgen05 attention CTA first wait
+  // this many ns on a barrier that nothing arrives on; the wait runs out, the CTA takes its
+  // abort path and the device error word reports a timeout.
+  uint32_t stall_test_ns;
 };
 
 struct Pointers {

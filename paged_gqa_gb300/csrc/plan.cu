@@ -293,6 +293,16 @@ __device__ __forceinline__ void plan_class(const Problem& p, const Pointers& ptr
   __syncthreads();
 }
 
+// A class without blocks: no items for any CTA.
+__device__ __forceinline__ void empty_class(const ClassPlan& cp) {
+  for (int c = threadIdx.x; c <= cp.num_ctas; c += blockDim.x) cp.cta_item_begin[c] = 0;
+  if (threadIdx.x == 0) {
+    *cp.n_blocks = 0;
+    *cp.n_items = 0;
+    *cp.total_tiles = 0;
+  }
+}
+
 __global__ void __launch_bounds__(kPlanThreads, 1)
 plan_kernel(Problem p, Pointers ptr, ClassPlan c0, ClassPlan c1) {
   __shared__ long long s_total;
@@ -314,9 +324,13 @@ plan_kernel(Problem p, Pointers ptr, ClassPlan c0, ClassPlan c1) {
     if (p.num_seqs > 0 && (ptr.qsl[0] != 0 || ptr.qsl[p.num_seqs] != p.T)) atomicOr(ptr.err, kErrBounds);
   }
   // Sequence info, once. Rows of invalid sequences are zeroed and flagged; they get no blocks.
+  // Which classes have any block at all: an empty class gets an empty plan at once.
+  int has_v = 0, has_p = 0;
   for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) {
     SeqInfo si = seq_info(p, ptr, s);
     if (s < kSeqCache) sm.seq[s] = make_int4(si.q0, si.qn, si.L, si.ok);
+    has_v |= blocks_per_head(si, p.G, 0) > 0;
+    has_p |= blocks_per_head(si, p.G, 1) > 0;
     if (!si.ok) {
       atomicOr(ptr.err, kErrBounds);
       int q0 = max(0, si.q0), q1 = min(p.T, max(q0, si.q0 + max(si.qn, 0)));
@@ -326,9 +340,10 @@ plan_kernel(Problem p, Pointers ptr, ClassPlan c0, ClassPlan c1) {
           for (int d = 0; d < kHeadDim; ++d) o[t * p.o_st + h * p.o_sh + d] = 0;
     }
   }
-  __syncthreads();
-  plan_class(p, ptr, c0, 0, sm);
-  plan_class(p, ptr, c1, 1, sm);
+  has_v = __syncthreads_or(has_v);
+  has_p = __syncthreads_or(has_p);
+  if (has_v) plan_class(p, ptr, c0, 0, sm); else empty_class(c0);
+  if (has_p) plan_class(p, ptr, c1, 1, sm); else empty_class(c1);
   if (threadIdx.x == 0 && s_overflow) {
     // Host-side bounds make this unreachable; flag it rather than run a partial plan.
     atomicOr(ptr.err, kErrBounds);

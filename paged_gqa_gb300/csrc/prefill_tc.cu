@@ -91,6 +91,7 @@ struct Misc {
   alignas(8) uint64_t k_full[kKStages], k_empty[kKStages], v_full[3], v_empty[3];
   uint64_t s_full[2], pv_done[2];
   uint64_t p_full, q_full, q_free, o_ready, o_free, drain[2];
+  uint64_t never;  // no thread ever arrives (the failure-path test waits on it)
   float qscale[2];
   float amax[kSoftWarps];
   uint32_t tmem_base;
@@ -180,6 +181,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     mbar_init(bar(ms.o_free), kSoftThreads);
     mbar_init(bar(ms.drain[0]), 1);
     mbar_init(bar(ms.drain[1]), 1);
+    mbar_init(bar(ms.never), 1);
     ms.abort_flag = 0;
     fence_mbar_init();
   }
@@ -261,7 +263,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
     if (lane == 0) {
       for (int s = 0; s < nst; ++s)
-        if (issued[s]) mbar_wait(bar(full[s]), (issued[s] - 1) & 1, abort_flag, ptr.err);
+        if (issued[s]) mbar_drain(bar(full[s]), (issued[s] - 1) & 1, abort_flag, ptr.err);
     }
     __syncwarp();
   } else if (warp == 1 || warp == kPVIssuerWarp) {
@@ -323,7 +325,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       // Every MMA this thread issued has completed before the CTA may release TMEM.
       uint64_t& drain = is_s ? ms.drain[0] : ms.drain[1];
       mma_commit(bar(drain));
-      mbar_wait(bar(drain), 0, abort_flag, ptr.err);
+      mbar_drain(bar(drain), 0, abort_flag, ptr.err);
     }
     __syncwarp();
   } else if (warp >= 2 && warp < kVProducerWarp) {
@@ -339,6 +341,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     const float2 q_cast = kQM == kQCast ? q_cast_scales(ptr.q_amax, p.q_amax_parts, lane) : make_float2(1.f, 1.f);
     bool bad = false;
     float m_ref = kMInit, l = 0.f;
+    // Failure-path test: a bounded wait on a barrier nothing arrives on runs out in every
+    // softmax thread (by its own limit or by the abort flag another thread raised); they
+    // then skip the items, so no Q is published, the MMA issuers give up on q_full / p_full
+    // and every producer drains the copies it issued.
+    const bool stalled = p.stall_test_ns && !mbar_wait(bar(ms.never), 0, abort_flag, ptr.err, p.stall_test_ns);
+    if (!stalled) {
 
     auto q_prep = [&](const Item& I, int ii) {
       const int pi = ii & 1;
@@ -632,6 +640,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         finish_split_block(p, ptr, cp, I.block, rb, gi, kSoftThreads, 10, &ms.merge_flag, ms.merge_w);
       }
     }
+    }  // !stalled
+    (void)bad;
   }
 
   tc_fence_before();

@@ -46,17 +46,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with the given parity to complete.
+// Bounded wait for the phase with the given parity to complete. Gives up at once (false)
+// when the CTA's abort flag is raised, or after limit_ns (then it records kErrTimeout and
+// raises the abort flag itself).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* err) {
+                                          uint32_t* err, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0u) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) break;
+      if (global_timer_ns() - t0 > limit_ns) break;
     }
+  }
+  atomicOr(err, kErrTimeout);
+  *abort_flag = 1;
+  return false;
+}
+
+// Wait for this thread's own asynchronous work (TMA copies, MMAs) signalled on `bar` before
+// the CTA releases its shared memory or TMEM. Unlike mbar_wait it does not give up when the
+// abort flag is raised (that work is in flight either way and completes by itself); it
+// is still bounded by kWaitLimitNs, after which it records kErrTimeout.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           uint32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) break;
   }
   atomicOr(err, kErrTimeout);
   *abort_flag = 1;

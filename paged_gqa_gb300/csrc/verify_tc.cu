@@ -117,6 +117,7 @@ struct Misc {
   alignas(8) uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[kPBufs], pv_done[kPBufs], q_full, q_free, o_ready, o_free, drain[2], merge_full;
+  uint64_t never;  // no thread ever arrives (the failure-path test waits on it)
   float qscale[2];
   float amax[kSoftWarps];
   uint32_t tmem_base;
@@ -207,6 +208,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     mbar_init(bar(ms.drain[0]), 1);
     mbar_init(bar(ms.drain[1]), 1);
     mbar_init(bar(ms.merge_full), 1);
+    mbar_init(bar(ms.never), 1);
     ms.abort_flag = 0;
     fence_mbar_init();
   }
@@ -241,6 +243,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     for (int n = 0; n < kCols; ++n) l[n] = 0.f;
     bool bad = false;
     uint32_t merge_phase = 0;  // phases of merge_full used so far
+    // Failure-path test: a bounded wait on a barrier nothing arrives on runs out in every
+    // softmax thread (by its own limit or by the abort flag another thread raised); they
+    // then skip the items, so no Q is published, the MMA issuers give up on q_full / p_full
+    // and every producer drains the copies it issued.
+    const bool stalled = p.stall_test_ns && !mbar_wait(bar(ms.never), 0, abort_flag, ptr.err, p.stall_test_ns);
+    if (!stalled) {
 
     auto q_prep = [&](const Item& I, int ii) {
       const int pi = ii & 1;
@@ -673,7 +681,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                 }
                 named_barrier(2, kSoftThreads);
               }
-              if (!mbar_wait(bar(ms.merge_full), merge_phase & 1, abort_flag, ptr.err)) bad = true;
+              // the bulk loads are this CTA's own: wait for them even after an abort, before the
+              // buffers are read or reloaded (and before the CTA may exit)
+              if (!mbar_drain(bar(ms.merge_full), merge_phase & 1, abort_flag, ptr.err)) bad = true;
               ++merge_phase;
               for (int idx = gi; idx < nr * (kHeadDim / 4); idx += kSoftThreads) {
                 const int r = idx / (kHeadDim / 4), d = (idx % (kHeadDim / 4)) * 4;
@@ -707,6 +717,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
       for (int n = 0; n < kCols; ++n) l[n] = 0.f;
     }
+    }  // !stalled
+    (void)bad;
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
     const bool k_prod = warp == 2 || warp == 3 || warp == 20;
@@ -797,7 +809,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       // Every issued copy has landed before the CTA may exit.
       if (lane == 0) {
         for (int s = 0; s < nst; ++s)
-          if (issued[s]) mbar_wait(bar(full[s]), (issued[s] - 1) & 1, abort_flag, ptr.err);
+          if (issued[s]) mbar_drain(bar(full[s]), (issued[s] - 1) & 1, abort_flag, ptr.err);
       }
       __syncwarp();
     } else if (warp == 0 || warp == 1) {
@@ -857,7 +869,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         // Every MMA this thread issued has completed before the CTA may release TMEM.
         uint64_t& drain = is_s ? ms.drain[0] : ms.drain[1];
         mma_commit(bar(drain));
-        mbar_wait(bar(drain), 0, abort_flag, ptr.err);
+        mbar_drain(bar(drain), 0, abort_flag, ptr.err);
       }
       __syncwarp();
     }

@@ -121,6 +121,11 @@ def test_empty_batch_is_a_no_op():
     assert _call(a) == 0
 
 
+def test_set_stall_test_roundtrip():
+    prev = pg.paged_gqa_set_stall_test(1000)
+    assert pg.paged_gqa_set_stall_test(prev) == 1000
+
+
 def test_set_path_roundtrip():
     prev = pg.paged_gqa_set_path(1)
     assert pg.paged_gqa_set_path(prev) == 1
