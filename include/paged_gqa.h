@@ -184,7 +184,9 @@ int paged_gqa_attn_quant_q(const pg_tensor* q, const pg_tensor* k_cache, const p
  *            K may be 0 (every row zero). Caller-owned, read only.
  * q must be bf16 and the caches e4m3 with the same strides (else PG_ERR_UNSUPPORTED /
  * PG_ERR_INVALID_ARG). Allocates nothing. A block-table entry out of range sets
- * PG_ERR_DEVICE_BOUNDS in the device error word and the key is skipped.
+ * PG_ERR_DEVICE_BOUNDS in the device error word and the key is skipped. Lists of 64 or
+ * more entries run on the tcgen05 kernel (four (token, kv head) units share a tile), shorter
+ * ones (and every call under paged_gqa_set_path(1)) on the warp-level kernel.
  */
 int paged_gqa_sparse_attn(const pg_tensor* q, const pg_tensor* k_cache, const pg_tensor* v_cache,
                           const pg_tensor* block_table, const pg_tensor* seq_lens,
@@ -269,7 +271,9 @@ int paged_gqa_set_stall_test(uint32_t wait_ns);
  * Host-side launch summary of the last successful call on this host thread, for
  * tests and the benchmark. out8 receives {verify CTAs, prefill CTAs, kernels
  * launched, path bits (2: tcgen05 verify, 4: tcgen05 prefill, 8: warp-MMA verify,
- * 16: warp-MMA prefill), verify block bound, prefill block bound, workspace bytes, 0}.
+ * 16: warp-MMA prefill, 32: tcgen05 sparse, 64: warp-MMA sparse), verify block bound,
+ * prefill block bound, workspace bytes, 0}. A sparse call sets only the launch count and
+ * the path bits.
  */
 int paged_gqa_last_plan(int64_t* out8);
 

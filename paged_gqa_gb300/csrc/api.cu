@@ -513,8 +513,21 @@ int paged_gqa_sparse_attn(const pg_tensor* q, const pg_tensor* k_cache, const pg
   a.score_scale_log2 = (float)((double)softmax_scale * (double)k_descale * 1.4426950408889634);
   a.out_scale = v_descale;
   a.err = ds->err;
-  e = launch_sparse(a, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");
+  // tcgen05 kernel for lists of at least two tiles' worth of keys; the warp-level kernel for
+  // shorter lists and under paged_gqa_set_path(1)
+  int used = 0;
+  if (g_path.load() == 0) {
+    const int r = launch_sparse_tc(a, ds->sms, p.stall_test_ns, reinterpret_cast<cudaStream_t>(stream));
+    if (r < 0) return fail(PG_ERR_CUDA, "tcgen05 sparse launch failed: %s", tc_last_error());
+    if (r == 1) used = 32;
+  }
+  if (!used) {
+    e = launch_sparse(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");
+    used = 64;
+  }
+  int64_t plan_info[8] = {0, 0, 1, used, 0, 0, 0, 0};
+  memcpy(t_last_plan, plan_info, sizeof plan_info);
   t_last_error.clear();
   return PG_OK;
 }

@@ -49,6 +49,11 @@ struct SparseArgs {
   uint32_t* err;
 };
 cudaError_t launch_sparse(const SparseArgs& a, cudaStream_t stream);
+// tcgen05 kernel of sparse attention (sparse_tc.cu): 1 if launched, 0 if the call is outside
+// what it handles (lists shorter than sparse_tc_min_keys()), -1 on a launch error (message
+// from tc_last_error()).
+int launch_sparse_tc(const SparseArgs& a, int sms, uint32_t stall_test_ns, cudaStream_t stream);
+int sparse_tc_min_keys();
 
 // Per-CTA maxima of |q| over a bf16 Q (q_amax.cu), q_amax_parts(sms) of them, for the
 // per-tensor cast of Q in the tcgen05 kernels.

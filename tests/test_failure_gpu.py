@@ -43,3 +43,21 @@ def test_a_wait_that_runs_out_reports_timeout_and_the_next_call_is_correct(which
     got = gu.run_library(case)
     assert pg.paged_gqa_last_plan()["path_bits"] & bits
     gu.check_full(case, got, f"after a timeout ({which})")
+
+
+def test_sparse_kernel_wait_that_runs_out_reports_timeout():
+    import paged_gqa_gb300 as pg
+    from tests.test_sparse_gpu import _oracle, _run
+    gen = torch.Generator().manual_seed(78)
+    spec = wl.random_small_spec(gen, group=12, num_kv_heads=2, page_size=64, q_lens=[6, 3], max_ctx=800,
+                                kv_dtype="e4m3", q_dtype="bf16")
+    case = wl.make_case(spec, device="cuda", seed=78, poison=True)
+    idx = wl.sparse_indices(case.spec, 200, device="cuda", seed=78)
+    prev = pg.paged_gqa_set_stall_test(200_000)
+    try:
+        _run(case, idx, check=False)
+        st = pg.paged_gqa_check_device_errors()
+    finally:
+        pg.paged_gqa_set_stall_test(prev)
+    assert st == PG_ERR_TIMEOUT, pg.paged_gqa_last_error()
+    gu.compare(_run(case, idx), _oracle(case, idx), "sparse after a timeout")

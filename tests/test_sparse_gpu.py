@@ -10,6 +10,9 @@ from tests import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 
+TC_MIN_KEYS = 64  # lists at least this long run on the tcgen05 kernel (path bit 32), else warp MMA (64)
+
+
 def _run(case, idx, out=None, check=True):
     import paged_gqa_gb300 as pg
     T, Hq = case.q.shape[0], case.q.shape[1]
@@ -19,7 +22,25 @@ def _run(case, idx, out=None, check=True):
                              case.query_start_loc, idx, case.k_descale, case.v_descale, case.softmax_scale, out)
     if check:
         assert pg.paged_gqa_check_device_errors() == 0, pg.paged_gqa_last_error()
+    if T > 0 and idx.shape[2] > 0:
+        bits = pg.paged_gqa_last_plan()["path_bits"]
+        path = pg.paged_gqa_set_path(0)  # read the current selection, then put it back
+        pg.paged_gqa_set_path(path)
+        want = 64 if path == 1 or idx.shape[2] < TC_MIN_KEYS else 32
+        assert bits == want, f"path bits {bits}, expected {want}"
     return out
+
+
+class warp_mma_path:
+    """Every sparse call inside runs on the warp-level kernel (paged_gqa_set_path(1))."""
+
+    def __enter__(self):
+        import paged_gqa_gb300 as pg
+        self.prev = pg.paged_gqa_set_path(1)
+
+    def __exit__(self, *exc):
+        import paged_gqa_gb300 as pg
+        pg.paged_gqa_set_path(self.prev)
 
 
 def _oracle(case, idx, rows=None):
@@ -54,15 +75,46 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("path", ["auto", "warp_mma"])
 @pytest.mark.parametrize("i", range(len(SMALL)))
-def test_small_cases_match_the_oracle(i):
+def test_small_cases_match_the_oracle(i, path):
     G, hkv, page, q_lens, ctx, K = SMALL[i]
     gen = torch.Generator().manual_seed(90 + i)
     spec = wl.random_small_spec(gen, group=G, num_kv_heads=hkv, page_size=page, q_lens=q_lens, max_ctx=ctx,
                                 kv_dtype="e4m3", q_dtype="bf16")
     case = wl.make_case(spec, device="cuda", seed=90 + i, poison=True)
     idx = _random_lists(case, K, 90 + i)
-    gu.compare(_run(case, idx), _oracle(case, idx), f"sparse case {i}")
+    ref = _oracle(case, idx)
+    if path == "auto":
+        gu.compare(_run(case, idx), ref, f"sparse case {i}")
+    else:
+        with warp_mma_path():
+            gu.compare(_run(case, idx), ref, f"sparse case {i}, warp MMA")
+
+
+# tcgen05 kernel shapes: units not a multiple of four (padding units), two head groups per
+# kv head, several kv heads, lists that are not a multiple of 32, and one whole tile only
+TC_CASES = [
+    # (group, kv heads, page, q_lens, max context, K)
+    (12, 2, 64, [3, 2], 700, 257),
+    (24, 1, 16, [5, 1, 2], 600, 96),
+    (3, 4, 32, [6, 1], 500, 64),
+    (16, 1, 128, [7], 1200, 301),
+    (6, 2, 16, [1, 1, 1, 1, 1], 900, 130),
+]
+
+
+@pytest.mark.parametrize("i", range(len(TC_CASES)))
+def test_tcgen05_sparse_shapes_match_the_oracle(i):
+    G, hkv, page, q_lens, ctx, K = TC_CASES[i]
+    gen = torch.Generator().manual_seed(190 + i)
+    spec = wl.random_small_spec(gen, group=G, num_kv_heads=hkv, page_size=page, q_lens=q_lens, max_ctx=ctx,
+                                kv_dtype="e4m3", q_dtype="bf16")
+    case = wl.make_case(spec, device="cuda", seed=190 + i, poison=True)
+    idx = _random_lists(case, K, 190 + i)
+    gu.compare(_run(case, idx), _oracle(case, idx), f"tcgen05 sparse case {i}")
+    idx = wl.sparse_indices(case.spec, K, device="cuda", seed=190 + i)
+    gu.compare(_run(case, idx), _oracle(case, idx), f"tcgen05 sparse case {i}, generated lists")
 
 
 def test_generated_top_k_lists_and_empty_lists():
