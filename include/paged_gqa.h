@@ -161,7 +161,7 @@ int paged_gqa_attn_noalloc(const pg_tensor* q, const pg_tensor* k_cache, const p
  *
  * Arguments are those of paged_gqa_attn, except: q must be bf16 and the caches e4m3
  * (else PG_ERR_UNSUPPORTED), and the tcgen05 path must be selected (paged_gqa_set_path
- * 0, the default; else PG_ERR_UNSUPPORTED). Uses the library-owned workspace like
+ * 0, the default, or 2; else PG_ERR_UNSUPPORTED). Uses the library-owned workspace like
  * paged_gqa_attn. Error behaviour as paged_gqa_attn.
  */
 int paged_gqa_attn_quant_q(const pg_tensor* q, const pg_tensor* k_cache, const pg_tensor* v_cache,
@@ -184,9 +184,9 @@ int paged_gqa_attn_quant_q(const pg_tensor* q, const pg_tensor* k_cache, const p
  *            K may be 0 (every row zero). Caller-owned, read only.
  * q must be bf16 and the caches e4m3 with the same strides (else PG_ERR_UNSUPPORTED /
  * PG_ERR_INVALID_ARG). Allocates nothing. A block-table entry out of range sets
- * PG_ERR_DEVICE_BOUNDS in the device error word and the key is skipped. Lists of 64 or
- * more entries run on the tcgen05 kernel (four (token, kv head) units share a tile), shorter
- * ones (and every call under paged_gqa_set_path(1)) on the warp-level kernel.
+ * PG_ERR_DEVICE_BOUNDS in the device error word and the key is skipped. Two kernels compute
+ * it: a warp-level one (the default) and a tcgen05 one for lists of 64 or more entries (four
+ * (token, kv head) units share a tile), selected by paged_gqa_set_path(2).
  */
 int paged_gqa_sparse_attn(const pg_tensor* q, const pg_tensor* k_cache, const pg_tensor* v_cache,
                           const pg_tensor* block_table, const pg_tensor* seq_lens,
@@ -248,8 +248,11 @@ int paged_gqa_check_device_errors(pg_stream_t stream);
 
 /*
  * Kernel path selection, for tests and sweeps (process-wide):
- *   0 = automatic (tcgen05 kernels where they apply, warp-level MMA otherwise)
+ *   0 = automatic: the dense calls use the tcgen05 kernels where they apply (e4m3 caches)
+ *       and warp-level MMA otherwise; sparse calls use the warp-level kernel (measured the
+ *       faster of the two on the sparse workloads)
  *   1 = warp-level MMA (mma.sync) kernel for every tile
+ *   2 = as 0, but sparse calls with lists of 64 or more entries use the tcgen05 kernel
  * Returns the previous value, or PG_ERR_INVALID_ARG.
  */
 int paged_gqa_set_path(int path);

@@ -310,7 +310,7 @@ int run(const Validated& val, const pg_tensor* k, const pg_tensor* v, void* ws, 
   int64_t plan_info[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   const int path = g_path.load();
   // Fast (tcgen05) kernels need an e4m3 cache; bf16 caches use the warp-MMA kernel.
-  const bool fast_ok = path == 0 && p.kv_is_fp8;
+  const bool fast_ok = path != 1 && p.kv_is_fp8;
   // Only the tcgen05 kernels cast Q per tensor; nothing else may stand in for them.
   if (p.q_cast && !fast_ok) return fail(PG_ERR_UNSUPPORTED, "quantising q needs the tcgen05 path");
   int launched = 0;
@@ -513,10 +513,13 @@ int paged_gqa_sparse_attn(const pg_tensor* q, const pg_tensor* k_cache, const pg
   a.score_scale_log2 = (float)((double)softmax_scale * (double)k_descale * 1.4426950408889634);
   a.out_scale = v_descale;
   a.err = ds->err;
-  // tcgen05 kernel for lists of at least two tiles' worth of keys; the warp-level kernel for
-  // shorter lists and under paged_gqa_set_path(1)
+  // The warp-level kernel by default: on the sparse workloads of "Tune sparse GQA prefill
+  // profile" it is the faster of the two (3.4 vs 4.4 ms on the TP1 shape; the tcgen05 kernel's
+  // row gather is bound by the latency of 16-byte copies from L2 with two K stages in
+  // flight). paged_gqa_set_path(2) selects the tcgen05 kernel for lists of at least two
+  // tiles' worth of keys.
   int used = 0;
-  if (g_path.load() == 0) {
+  if (g_path.load() == 2) {
     const int r = launch_sparse_tc(a, ds->sms, p.stall_test_ns, reinterpret_cast<cudaStream_t>(stream));
     if (r < 0) return fail(PG_ERR_CUDA, "tcgen05 sparse launch failed: %s", tc_last_error());
     if (r == 1) used = 32;
@@ -570,7 +573,7 @@ int paged_gqa_check_device_errors(pg_stream_t stream) {
 }
 
 int paged_gqa_set_path(int path) {
-  if (path < 0 || path > 1) return fail(PG_ERR_INVALID_ARG, "path must be 0 or 1");
+  if (path < 0 || path > 2) return fail(PG_ERR_INVALID_ARG, "path must be 0, 1 or 2");
   return g_path.exchange(path);
 }
 

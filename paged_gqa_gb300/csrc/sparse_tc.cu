@@ -28,9 +28,10 @@
 //     has the same number of tiles (the list length), so there is no split and no merge.
 //
 // Warp roles (768 threads): warp 0 = S issuer (+ TMEM owner), warp 1 = P.V issuer, warps
-// 2-3 idle, warps 4-19 = softmax and epilogue, warps 20-21 = K gatherers, 22-23 = V
-// gatherers (gatherer warp w of an operand fills stage w, i.e. every other tile). Shared
-// memory: Q hi/lo 32 KB, 2 K + 2 V stages of 32 KB, two block-diagonal P buffers of 16 KB.
+// 4-19 = softmax and epilogue, warps 20-21 = K gatherers, warps 22, 23, 2, 3 = V gatherers
+// (V stages are held until P.V completes, so V gets more warps and stages).
+// Shared memory: Q hi/lo 32 KB, 2 K + 3 V stages of 32 KB, two block-diagonal P buffers of
+// 16 KB (227 KB in all).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -59,11 +60,9 @@ constexpr int kThreads = 768;
 constexpr int kSoftWarps = 16;
 constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kSoftWarp0 = 4;
-constexpr int kKGather0 = 20, kVGather0 = 22;  // two gatherer warps per operand
-constexpr int kGatherThreads = 32;              // arrivals on a stage's full barrier (one warp)
 constexpr int kQChunks = kRows * 16 / kSoftThreads;  // Q chunks of 16 elements per softmax thread
 static_assert(kQChunks * kSoftThreads == kRows * 16, "Q chunks");
-constexpr int kKStages = 2, kVStages = 2, kPBufs = 2;
+constexpr int kKStages = 2, kVStages = 3, kPBufs = 2;
 constexpr float kTau = 4.f, kSigma = 4.f, kMInit = -1.0e30f;
 
 constexpr uint32_t kQHalf = 2 * kRows * 128;   // [Q_hi 64 rows | Q_lo 64 rows] x 128 B
@@ -103,6 +102,7 @@ struct Misc {
 };
 static_assert(offsetof(Misc, alpha) % 16 == 0 && offsetof(Misc, k_full) % 8 == 0, "Misc alignment");
 constexpr size_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
+static_assert(kSmemBytes <= 232448, "fits the 227 KB of dynamic shared memory a CTA may use");
 
 // A unit's token, kv head, first q head and rows, its sequence and causal limit. Called by a
 // whole converged warp (the sequence search is warp-cooperative); every lane gets the result.
@@ -135,6 +135,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void st_shared_zero16(uint32_t dst) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
@@ -187,25 +188,25 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseArgs a, in
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKStages; ++s) {
-      mbar_init(bar(ms.k_full[s]), kGatherThreads);
+      mbar_init(bar(ms.k_full[s]), 2);  // the K team's warps
       mbar_init(bar(ms.k_empty[s]), 1);
     }
     for (int s = 0; s < kVStages; ++s) {
-      mbar_init(bar(ms.v_full[s]), kGatherThreads);
+      mbar_init(bar(ms.v_full[s]), 4);  // the V team's warps
       mbar_init(bar(ms.v_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(ms.s_full[b]), 1);
-      mbar_init(bar(ms.s_free[b]), kSoftThreads);
+      mbar_init(bar(ms.s_free[b]), kSoftWarps);
     }
     for (int b = 0; b < kPBufs; ++b) {
-      mbar_init(bar(ms.p_full[b]), kSoftThreads);
+      mbar_init(bar(ms.p_full[b]), kSoftWarps);
       mbar_init(bar(ms.pv_done[b]), 1);
     }
-    mbar_init(bar(ms.q_full), kSoftThreads);
+    mbar_init(bar(ms.q_full), kSoftWarps);
     mbar_init(bar(ms.q_free), 1);
     mbar_init(bar(ms.o_ready), 1);
-    mbar_init(bar(ms.o_free), kSoftThreads);
+    mbar_init(bar(ms.o_free), kSoftWarps);
     mbar_init(bar(ms.drain[0]), 1);
     mbar_init(bar(ms.drain[1]), 1);
     mbar_init(bar(ms.never), 1);
@@ -235,13 +236,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseArgs a, in
     const int group_bar = 3 + j4;             // the four warps (one per unit) of subgroup j4
     const int key = kUnitKeys * u + lane;     // tile-local key = TMEM lane of S
     const uint32_t lane_addr = (uint32_t)(u * 32) << 16;
-    const bool stalled = stall_test_ns && !mbar_wait(bar(ms.never), 0, abort_flag, a.err, (uint64_t)stall_test_ns);
+    bool stalled = false;
+    if (stall_test_ns) {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(bar(ms.never), 0, abort_flag, a.err, (uint64_t)stall_test_ns);
+      stalled = __shfl_sync(0xffffffffu, ok, 0) == 0;
+    }
     if (!stalled) {
     float m[4], mo[4], l[4];
 
     auto q_prep = [&](long long qi, int ii) {
       const int pi = ii & 1;
-      if (ii >= 1) mbar_wait(bar(ms.q_free), (ii - 1) & 1, abort_flag, a.err);
+      if (ii >= 1) mbar_wait_warp(bar(ms.q_free), (ii - 1) & 1, abort_flag, a.err, lane);
       if (sw < kQuad) {  // one warp per unit of the quad
         const Unit U = unit_info(a, qi * kQuad + sw, lane);
         if (lane == 0) {
@@ -309,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseArgs a, in
       }
       if (gi == 0) ms.qscale[pi] = ldexpf(1.f, -sig);
       fence_proxy_async_smem();
-      mbar_arrive(bar(ms.q_full));
+      mbar_arrive_warp(bar(ms.q_full), lane);
     };
 
     int ii = 0;
@@ -334,8 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseArgs a, in
         const int b = g & 1;
         const uint32_t vst = g % kVStages;
         float sh[4], sl[4], s[4], x[4];
-        mbar_wait(bar(ms.s_full[b]), (g >> 1) & 1, abort_flag, a.err);
-        mbar_wait(bar(ms.v_full[vst]), (g / kVStages) & 1, abort_flag, a.err);  // the keys' validity bits
+        mbar_wait_warp(bar(ms.s_full[b]), (g >> 1) & 1, abort_flag, a.err, lane);
+        mbar_wait_warp(bar(ms.v_full[vst]), (g / kVStages) & 1, abort_flag, a.err, lane);  // the keys' validity bits
         tc_fence_after();
         tmem_ld4(tmem + lane_addr + kColS + b * 128 + row0, sh);
         tmem_ld4(tmem + lane_addr + kColS + b * 128 + kRows + row0, sl);
@@ -367,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseArgs a, in
           named_barrier(group_bar, 128);
         }
         tc_fence_before();
-        mbar_arrive(bar(ms.s_free[b]));
+        mbar_arrive_warp(bar(ms.s_free[b]), lane);
         // P = 2^x in f16, split into e4m3 hi + lo (this key, 4 rows); row sums in fp32
         uint32_t ph, pl;
         __half2 s01, s23;
@@ -381,8 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseArgs a, in
         }
         // P buffer g & 1 is free once P.V(g-2) has completed; O^T may be rescaled once
         // P.V(g-1) has.
-        if (g >= 2) mbar_wait(bar(ms.pv_done[g & 1]), ((g >> 1) - 1) & 1, abort_flag, a.err);
-        if (rescale && j > 0) mbar_wait(bar(ms.pv_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, abort_flag, a.err);
+        if (g >= 2) mbar_wait_warp(bar(ms.pv_done[g & 1]), ((g >> 1) - 1) & 1, abort_flag, a.err, lane);
+        if (rescale && j > 0) mbar_wait_warp(bar(ms.pv_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, abort_flag, a.err, lane);
         tc_fence_after();
         if (rescale && j > 0) {
           // O^T columns of the subgroup's 16 rows (4 of each unit), both d-halves and parts
@@ -411,13 +417,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseArgs a, in
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(ms.p_full[g & 1]));
+        mbar_arrive_warp(bar(ms.p_full[g & 1]), lane);
       }
       // Q of the next quad while this quad's last P.V runs
       if (qi + 1 < quad_end) q_prep(qi + 1, ii + 1);
 
       // ---------------------------------------------------------- epilogue
-      mbar_wait(bar(ms.o_ready), ii & 1, abort_flag, a.err);
+      mbar_wait_warp(bar(ms.o_ready), ii & 1, abort_flag, a.err, lane);
       tc_fence_after();
       // row sums over this warp's 32 keys, then 1 / l per row
 #pragma unroll
@@ -451,59 +457,63 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseArgs a, in
         }
       }
       tc_fence_before();
-      mbar_arrive(bar(ms.o_free));
+      mbar_arrive_warp(bar(ms.o_free), lane);
     }
     }  // !stalled
   } else {
-    const bool k_gather = warp == kKGather0 || warp == kKGather0 + 1;
-    const bool v_gather = warp == kVGather0 || warp == kVGather0 + 1;
-    if (k_gather || v_gather) {
+    const int kt = warp == 20 ? 0 : warp == 21 ? 1 : -1;                               // K team member
+    const int vt = warp == 22 ? 0 : warp == 23 ? 1 : warp == 2 ? 2 : warp == 3 ? 3 : -1;  // V team member
+    if (kt >= 0 || vt >= 0) {
       // ------------------------------------------------------------ gatherers (K, V)
-      // The two gatherer warps of an operand take alternate tiles, so warp w always fills
-      // stage w. Per tile, lane l looks up entry j * 32 + l of each of the quad's 4 units
-      // (the list, then the block table), the warp copies the 128 rows, two 256-byte rows
-      // per instruction and 16 bytes per lane, into the swizzled stage, then waits for its
-      // own copies, makes them visible to the tensor core (proxy fence) and arrives on the
-      // stage's full barrier. The next tile's lookups are in flight while the copies run.
-      const bool is_k = k_gather;
-      const int w = is_k ? warp - kKGather0 : warp - kVGather0;  // = the stage this warp fills
+      // Two teams walk every tile in order: the K team (2 warps, two units each) and the V
+      // team (4 warps, one unit each). Per tile, lane l looks up entry j * 32 + l of the
+      // warp's units (the list, then the block table); each group of 16 keys is copied with
+      // lane pair (2k, 2k + 1) owning key k: one shuffle for the row offset, then 8 cp.async
+      // of 16 bytes per lane, a warp instruction moving 32 contiguous bytes of each of 16
+      // rows. A tile is published once the warp has issued the next one (two tiles in
+      // flight per warp): wait for all but the newest copy group, make the copies visible to
+      // the tensor core (proxy fence), arrive once on the stage's full barrier. The next
+      // tile's lookups are in flight while the copies run.
+      const bool is_k = kt >= 0;
+      const int nu = is_k ? 2 : 1;              // units this warp copies per tile
+      const int u0 = is_k ? 2 * kt : vt;        // its first unit
+      const int nst = is_k ? kKStages : kVStages;
       const uint8_t* base = is_k ? a.k : a.v;
-      const uint32_t stage = sbase + (is_k ? kOffK : kOffV) + w * kKVTile;
-      uint64_t& full = is_k ? ms.k_full[w] : ms.v_full[w];
-      uint64_t& empty = is_k ? ms.k_empty[w] : ms.v_empty[w];
-      static_assert(kKStages == 2 && kVStages == 2, "one stage per gatherer warp");
+      const uint32_t region = sbase + (is_k ? kOffK : kOffV);
+      uint64_t* full = is_k ? ms.k_full : ms.v_full;
+      uint64_t* empty = is_k ? ms.k_empty : ms.v_empty;
       const int pmask = a.P - 1;
       const long long total = (quad_end - quad_begin) * NT;  // tiles of this CTA
-      Unit U[kQuad];
+      Unit U[2];
       long long uq = -1;  // quad whose units U holds
       auto load_units = [&](long long qi) {
         if (qi == uq) return;
-#pragma unroll
-        for (int v = 0; v < kQuad; ++v) U[v] = unit_info(a, qi * kQuad + v, lane);
+        U[0] = unit_info(a, qi * kQuad + u0, lane);
+        if (is_k) U[1] = unit_info(a, qi * kQuad + u0 + 1, lane);
         uq = qi;
       };
       // list entries of tile g (lane l: entry j * 32 + l of each unit), -1 past the list
-      auto entries = [&](long long g, int (&e)[kQuad]) {
+      auto entries = [&](long long g, int (&e)[2]) {
         load_units(quad_begin + g / NT);
         const int i = (int)(g % NT) * kUnitKeys + lane;
 #pragma unroll
-        for (int v = 0; v < kQuad; ++v)
-          e[v] = (U[v].ok && i < a.K)
+        for (int v = 0; v < 2; ++v)
+          e[v] = (v < nu && U[v].ok && i < a.K)
                      ? __ldg(a.idx + (long long)U[v].t * a.idx_st + (long long)U[v].kvh * a.idx_sh + i)
                      : -1;
       };
-      auto pages = [&](const int (&e)[kQuad], int (&pg)[kQuad]) {
+      auto pages = [&](const int (&e)[2], int (&pg)[2]) {
 #pragma unroll
-        for (int v = 0; v < kQuad; ++v)
+        for (int v = 0; v < 2; ++v)
           pg[v] = (e[v] >= 0 && e[v] <= U[v].lim && (e[v] >> a.p_shift) < a.W)
                       ? __ldg(a.bt + (long long)U[v].s * a.bt_stride + (e[v] >> a.p_shift))
                       : -1;
       };
       // byte offset of each entry's row for its unit's kv head, or -1 (unused: padding, past
       // the causal limit; a listed position past W * P or a bad page also sets the error word)
-      auto offsets = [&](const int (&e)[kQuad], const int (&pg)[kQuad], long long (&o)[kQuad]) {
+      auto offsets = [&](const int (&e)[2], const int (&pg)[2], long long (&o)[2]) {
 #pragma unroll
-        for (int v = 0; v < kQuad; ++v) {
+        for (int v = 0; v < 2; ++v) {
           o[v] = -1;
           if (e[v] < 0 || e[v] > U[v].lim) continue;
           if ((e[v] >> a.p_shift) >= a.W) {
@@ -517,65 +527,72 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseArgs a, in
           o[v] = (long long)pg[v] * a.kv_sb + (long long)(e[v] & pmask) * a.kv_sp + (long long)U[v].kvh * a.kv_sh;
         }
       };
-      long long o[kQuad];
-      {
-        int e[kQuad], pg[kQuad];
-        if (w < total) {
-          entries(w, e);
-          pages(e, pg);
-          offsets(e, pg, o);
-        }
+      long long o[2] = {-1, -1};
+      if (total > 0) {
+        int e[2], pg[2];
+        entries(0, e);
+        pages(e, pg);
+        offsets(e, pg, o);
       }
-      uint32_t n = 0;  // tiles this warp has filled
-      for (long long g = w; g < total; g += 2, ++n) {
-        // the lookups of this warp's next tile: entries now, pages after the copies are issued
-        int e[kQuad], pg[kQuad];
-        const bool more = g + 2 < total;
-        long long next_q = -1;
-        if (more) {
-          next_q = quad_begin + (g + 2) / NT;
-          if (next_q == uq) entries(g + 2, e);  // (a new quad's units are loaded after the copies)
-        }
+      const int half_lane = lane >> 1, par = lane & 1;
+      int pending = -1;  // stage whose copies are issued but not yet published
+      for (long long g = 0; g < total; ++g) {
+        // the lookups of the next tile: entries now, pages after the copies are issued
+        int e[2], pg[2];
+        const bool more = g + 1 < total;
+        const long long next_q = more ? quad_begin + (g + 1) / NT : -1;
+        if (more && next_q == uq) entries(g + 1, e);  // (a new quad's units are loaded after the copies)
+        const uint32_t st = (uint32_t)(g % nst);
         int ok = 1;
-        if (lane == 0) ok = mbar_wait(bar(empty), (n & 1) ^ 1, abort_flag, a.err);
+        if (lane == 0) ok = mbar_wait(bar(empty[st]), (uint32_t)((g / nst) & 1) ^ 1u, abort_flag, a.err);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-#pragma unroll 4
-        for (int i = 0; i < kTileKeys / 2; ++i) {
-          const int key = 2 * i + (lane >> 4);  // tile-local key: unit key / 32, entry key % 32
-          const int ch = lane & 15;             // 16-byte chunk of its 256-byte row
-          const int v = i / (kUnitKeys / 2);    // the same unit for the whole warp
-          const long long src = v == 0 ? o[0] : v == 1 ? o[1] : v == 2 ? o[2] : o[3];
-          const long long off = shfl_off(src, key & 31);
-          const uint32_t dst = stage + (ch >> 3) * kKVHalf + key * 128 + (((ch & 7) ^ (key & 7)) << 4);
-          if (off >= 0) {
-            cp_async16(dst, base + off + ch * 16);
-          } else if (!is_k) {
-            st_shared_zero16(dst);  // an unused key's V row: zeros (0 x stale data could be NaN)
+        const uint32_t stage = region + st * kKVTile;
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+          if (v >= nu) break;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {                       // two groups of 16 keys per unit
+            const int key = kUnitKeys * (u0 + v) + 16 * h + half_lane;  // tile-local key of this lane pair
+            const long long off = shfl_off(o[v], 16 * h + half_lane);
+            const uint32_t row = stage + key * 128;
+            const int sw = key & 7;
+            if (off >= 0) {
+              const uint8_t* gsrc = base + off + par * 16;
+#pragma unroll
+              for (int m = 0; m < 8; ++m)  // chunk c = 2m + par: half c >> 3, 16-byte slot c & 7
+                cp_async16(row + (m >> 2) * kKVHalf + ((((2 * m + par) & 7) ^ sw) << 4), gsrc + m * 32);
+            } else if (!is_k) {
+#pragma unroll
+              for (int m = 0; m < 8; ++m)  // an unused key's V row: zeros (0 x stale data could be NaN)
+                st_shared_zero16(row + (m >> 2) * kKVHalf + ((((2 * m + par) & 7) ^ sw) << 4));
+            }
           }
         }
         cp_async_commit();
         if (!is_k) {
-          uint32_t bits[kQuad];
-#pragma unroll
-          for (int v = 0; v < kQuad; ++v) bits[v] = __ballot_sync(0xffffffffu, o[v] >= 0);
-          if (lane == 0) {
-#pragma unroll
-            for (int v = 0; v < kQuad; ++v) ms.vval[w][v] = bits[v];
-          }
+          const uint32_t bits = __ballot_sync(0xffffffffu, o[0] >= 0);
+          if (lane == 0) ms.vval[st][vt] = bits;
         }
+        if (pending >= 0) {
+          cp_async_wait1();  // the previous tile's copies have landed
+          fence_proxy_async_smem();
+          mbar_arrive_warp(bar(full[pending]), lane);
+        }
+        pending = (int)st;
         if (more) {
-          if (next_q != uq) entries(g + 2, e);
+          if (next_q != uq) entries(g + 1, e);
           pages(e, pg);
+          offsets(e, pg, o);
         }
-        cp_async_wait0();  // this lane's copies of the tile have landed
-        fence_proxy_async_smem();
-        mbar_arrive(bar(full));
-        if (more) offsets(e, pg, o);
       }
-      // Every issued copy has landed (cp_async_wait0 follows every tile's copies) before
-      // the CTA may exit.
+      // Every issued copy has landed before the last tile is published and before the CTA
+      // may exit (also after an abort).
       cp_async_wait0();
+      if (pending >= 0) {
+        fence_proxy_async_smem();
+        mbar_arrive_warp(bar(full[pending]), lane);
+      }
       __syncwarp();
     } else if (warp == 0 || warp == 1) {
       // ------------------------------------------------------------ MMA issuers

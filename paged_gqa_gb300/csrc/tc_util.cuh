@@ -65,6 +65,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   return false;
 }
 
+// mbar_wait by one lane of a converged warp while the other lanes wait at __syncwarp (which
+// orders their later accesses after lane 0's acquire): one poller per warp instead of 32, so
+// warps that wait do not flood the shared-memory pipe that other warps' copies, shuffles and
+// barrier arrivals use. Every lane gets the result.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               uint32_t* err, int lane) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(bar, parity, abort_flag, err);
+  __syncwarp();
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// One arrival on `bar` for the whole warp, after every lane's earlier accesses (ordered by
+// __syncwarp before lane 0's release). The barrier then counts warps, not threads.
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
 // Wait for this thread's own asynchronous work (TMA copies, MMAs) signalled on `bar` before
 // the CTA releases its shared memory or TMEM. Unlike mbar_wait it does not give up when the
 // abort flag is raised (that work is in flight either way and completes by itself); it

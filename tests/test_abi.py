@@ -129,6 +129,8 @@ def test_set_stall_test_roundtrip():
 def test_set_path_roundtrip():
     prev = pg.paged_gqa_set_path(1)
     assert pg.paged_gqa_set_path(prev) == 1
+    assert pg.paged_gqa_set_path(2) == prev
+    assert pg.paged_gqa_set_path(prev) == 2
     with pytest.raises(pg.PagedGQAError):
         pg.paged_gqa_set_path(7)
 

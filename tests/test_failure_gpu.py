@@ -53,11 +53,15 @@ def test_sparse_kernel_wait_that_runs_out_reports_timeout():
                                 kv_dtype="e4m3", q_dtype="bf16")
     case = wl.make_case(spec, device="cuda", seed=78, poison=True)
     idx = wl.sparse_indices(case.spec, 200, device="cuda", seed=78)
+    prev_path = pg.paged_gqa_set_path(2)  # the tcgen05 sparse kernel
     prev = pg.paged_gqa_set_stall_test(200_000)
     try:
         _run(case, idx, check=False)
         st = pg.paged_gqa_check_device_errors()
     finally:
         pg.paged_gqa_set_stall_test(prev)
-    assert st == PG_ERR_TIMEOUT, pg.paged_gqa_last_error()
-    gu.compare(_run(case, idx), _oracle(case, idx), "sparse after a timeout")
+    try:
+        assert st == PG_ERR_TIMEOUT, pg.paged_gqa_last_error()
+        gu.compare(_run(case, idx), _oracle(case, idx), "sparse after a timeout")
+    finally:
+        pg.paged_gqa_set_path(prev_path)

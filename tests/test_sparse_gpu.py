@@ -10,7 +10,7 @@ from tests import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 
-TC_MIN_KEYS = 64  # lists at least this long run on the tcgen05 kernel (path bit 32), else warp MMA (64)
+TC_MIN_KEYS = 64  # under path 2, lists at least this long run on the tcgen05 kernel (path bit 32)
 
 
 def _run(case, idx, out=None, check=True):
@@ -26,21 +26,33 @@ def _run(case, idx, out=None, check=True):
         bits = pg.paged_gqa_last_plan()["path_bits"]
         path = pg.paged_gqa_set_path(0)  # read the current selection, then put it back
         pg.paged_gqa_set_path(path)
-        want = 64 if path == 1 or idx.shape[2] < TC_MIN_KEYS else 32
+        want = 32 if path == 2 and idx.shape[2] >= TC_MIN_KEYS else 64
         assert bits == want, f"path bits {bits}, expected {want}"
     return out
 
 
-class warp_mma_path:
-    """Every sparse call inside runs on the warp-level kernel (paged_gqa_set_path(1))."""
+class kernel_path:
+    """Calls inside run under paged_gqa_set_path(path): 1 = warp-level kernel everywhere,
+    2 = the tcgen05 sparse kernel for lists of TC_MIN_KEYS or more."""
+
+    def __init__(self, path):
+        self.path = path
 
     def __enter__(self):
         import paged_gqa_gb300 as pg
-        self.prev = pg.paged_gqa_set_path(1)
+        self.prev = pg.paged_gqa_set_path(self.path)
 
     def __exit__(self, *exc):
         import paged_gqa_gb300 as pg
         pg.paged_gqa_set_path(self.prev)
+
+
+@pytest.fixture(autouse=True)
+def tcgen05_sparse():
+    """Every sparse test runs with the tcgen05 sparse kernel selected (path 2) unless it
+    selects another path itself; the default path's kernel is covered by the "auto" cases."""
+    with kernel_path(2):
+        yield
 
 
 def _oracle(case, idx, rows=None):
@@ -75,7 +87,7 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("path", ["auto", "warp_mma"])
+@pytest.mark.parametrize("path", [2, 0, 1])
 @pytest.mark.parametrize("i", range(len(SMALL)))
 def test_small_cases_match_the_oracle(i, path):
     G, hkv, page, q_lens, ctx, K = SMALL[i]
@@ -85,11 +97,8 @@ def test_small_cases_match_the_oracle(i, path):
     case = wl.make_case(spec, device="cuda", seed=90 + i, poison=True)
     idx = _random_lists(case, K, 90 + i)
     ref = _oracle(case, idx)
-    if path == "auto":
-        gu.compare(_run(case, idx), ref, f"sparse case {i}")
-    else:
-        with warp_mma_path():
-            gu.compare(_run(case, idx), ref, f"sparse case {i}, warp MMA")
+    with kernel_path(path):
+        gu.compare(_run(case, idx), ref, f"sparse case {i}, path {path}")
 
 
 # tcgen05 kernel shapes: units not a multiple of four (padding units), two head groups per
@@ -163,13 +172,15 @@ def test_bad_page_is_flagged_and_the_key_skipped():
     gu.compare(got, _oracle(case, dropped), "bad page skipped")
 
 
-def test_sparse_prefill_workload_sampled_rows():
+@pytest.mark.parametrize("path", [2, 0])
+def test_sparse_prefill_workload_sampled_rows(path):
     """The sparse page's TP1 shape: 8192 new tokens on a 32768-token context, 24 q / 2 kv
     heads, 2051 selected positions per (token, kv head); sampled rows and the end tokens."""
     spec = wl.sparse_spec(1)
     case = wl.make_case(spec, device="cuda", seed=0, poison=True)
     idx = wl.sparse_indices(spec, wl.SPARSE_TOPK, device="cuda", seed=0)
-    got = _run(case, idx).reshape(-1, wl.HEAD_DIM)
+    with kernel_path(path):
+        got = _run(case, idx).reshape(-1, wl.HEAD_DIM)
     Hq = spec.num_q_heads
     gen = torch.Generator().manual_seed(1)
     rows = torch.cat([torch.arange(Hq), torch.randperm(spec.total_q * Hq, generator=gen)[:400],
