@@ -187,7 +187,8 @@ class ClockSampler:
 
 def kernel_source_hash(cls_kind: str) -> str:
     names = {"verify": ["verify_tc.cu"], "prefill": ["prefill_tc.cu"], "portable": ["portable.cu"],
-             "cache_write": ["cache_write.cu"]}[cls_kind]
+             "cache_write": ["cache_write.cu"], "bf16": ["bf16_tc.cu"], "sparse": ["sparse.cu"],
+             "sparse_tc": ["sparse_tc.cu"]}[cls_kind]
     h = hashlib.sha256()
     for n in names + ["common.cuh", "device_util.cuh", "tc_util.cuh"]:
         p = os.path.join(ROOT, "paged_gqa_gb300", "csrc", n)
@@ -282,9 +283,13 @@ def _dominant(spec, config_index):
     return kind, cls
 
 
-def _kernel_kind(plan, cls, kind):
+def _kernel_kind(plan, cls, kind, spec=None):
     """Name of the class-`cls` kernel the last call ran (its traffic.json key prefix)."""
-    return ("verify" if cls == 0 else "prefill") if plan["path_bits"] & (2 << cls) else "portable"
+    if not plan["path_bits"] & (2 << cls):
+        return "portable"
+    if spec is not None and spec.kv_dtype == "bf16":
+        return "bf16"
+    return "verify" if cls == 0 else "prefill"
 
 
 def extra_config(pg, args, idx, dev, flush, local, world, quant_q):
@@ -312,7 +317,7 @@ def extra_config(pg, args, idx, dev, flush, local, world, quant_q):
          "value": round(per / (med / 1e3), 3), "unit": "GB/s" if kind == "hbm" else "TFLOP/s",
          "us_per_call": round(med * 1e3, 2), "us_per_call_mean": round(mean * 1e3, 2),
          "kernel_us_median": round(statistics.median(kern_ms) * 1e3, 2),
-         "roofline": _roofline(spec, kind, sum(kern_ms) / K, _kernel_kind(plan, cls, kind)),
+         "roofline": _roofline(spec, kind, sum(kern_ms) / K, _kernel_kind(plan, cls, kind, spec)),
          "path_bits": int(plan["path_bits"]), "clocks": clocks, "kv_bytes": spec.kv_bytes, "flops": spec.flops}
     if kind == "tensor":
         # the attainable bound with P.V at f16 precision: half the FLOPs at the FP8 rate and
@@ -398,7 +403,7 @@ def run_ours(args, rank, world, local):
     per_step = spec.kv_bytes / 1e9 if kind == "hbm" else spec.flops / 1e12
     unit = "GB/s" if kind == "hbm" else "TFLOP/s"
     value = whole_job_value(per_step, world, step_ms)
-    kernel_kind = _kernel_kind(plan, dominant_cls, kind)
+    kernel_kind = _kernel_kind(plan, dominant_cls, kind, spec)
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "ms_per_step_mean": round(step_mean_ms, 5),

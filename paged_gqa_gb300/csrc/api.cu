@@ -309,8 +309,10 @@ int run(const Validated& val, const pg_tensor* k, const pg_tensor* v, void* ws, 
   (void)ws_bytes;
   int64_t plan_info[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   const int path = g_path.load();
-  // Fast (tcgen05) kernels need an e4m3 cache; bf16 caches use the warp-MMA kernel.
+  // tcgen05 kernels: the verify and prefill kernels for e4m3 caches, the bf16 kernel (both
+  // classes) for a bf16 q with bf16 caches; the warp-MMA kernel under paged_gqa_set_path(1).
   const bool fast_ok = path != 1 && p.kv_is_fp8;
+  const bool bf16_ok = path != 1 && !p.kv_is_fp8 && !p.q_is_fp8;
   // Only the tcgen05 kernels cast Q per tensor; nothing else may stand in for them.
   if (p.q_cast && !fast_ok) return fail(PG_ERR_UNSUPPORTED, "quantising q needs the tcgen05 path");
   int launched = 0;
@@ -331,11 +333,13 @@ int run(const Validated& val, const pg_tensor* k, const pg_tensor* v, void* ws, 
     bool done = false;
     cudaEvent_t ev0 = g_ev_start[c].load(), ev1 = g_ev_stop[c].load();
     if (ev0 && (e = cudaEventRecord(ev0, stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if (fast_ok) {
+    if (fast_ok || bf16_ok) {
       // the prefill-class kernel follows the verify-class one as a programmatic dependent
       // (when that one is a tcgen05 kernel too and no event sits between them)
-      int r = (c == 0) ? launch_verify_tc(p, ptr, cp[c], k, v, ds->sms, stream)
-                       : launch_prefill_tc(p, ptr, cp[c], k, v, ds->sms, stream, (used & 2) && !ev0 && !prev_ev);
+      const bool dependent = c == 1 && (used & 2) && !ev0 && !prev_ev;
+      int r = bf16_ok ? launch_bf16_tc(p, ptr, cp[c], k, v, stream, dependent)
+              : (c == 0) ? launch_verify_tc(p, ptr, cp[c], k, v, ds->sms, stream)
+                         : launch_prefill_tc(p, ptr, cp[c], k, v, ds->sms, stream, dependent);
       if (r < 0) return fail(PG_ERR_CUDA, "tcgen05 %s launch failed: %s", c == 0 ? "verify" : "prefill",
                              tc_last_error());
       if (r == 1) {

@@ -75,7 +75,7 @@ bool encode_cache_tmap(CUtensorMap* m, const pg_tensor* t, int P);
 
 }  // namespace
 
-// 4-D map over an e4m3 cache [NB, P, Hkv, 256] (see encode_cache_tmap), from the cache of
+// 4-D map over a cache [NB, P, Hkv, 256] (see encode_cache_tmap), from the cache of
 // recent maps when the same tensor view was seen before.
 bool make_cache_tmap(CUtensorMap* m, const pg_tensor* t, int P) {
   TmapKey k{};
@@ -104,21 +104,27 @@ bool make_cache_tmap(CUtensorMap* m, const pg_tensor* t, int P) {
 
 namespace {
 
-// 4-D map over an e4m3 cache [NB, P, Hkv, 256]: box = one d-half (128 B) x 1 head x P rows
-// x 1 page, 128-byte swizzle, so one box lands a page's half-rows in the layout the MMA
-// descriptors expect (8-row atoms of 128 B).
+// 4-D map over a cache [NB, P, Hkv, 256]: box = 128 bytes of d x 1 head x the page's rows
+// x 1 page, 128-byte swizzle, so one box lands those rows in the layout the MMA descriptors
+// expect (8-row atoms of 128 B).
 bool encode_cache_tmap(CUtensorMap* m, const pg_tensor* t, int P) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     set_tc_error("cuTensorMapEncodeTiled unavailable");
     return false;
   }
+  // e4m3: a box is one 128-byte d-half of a page; bf16: one 128-byte d-quarter of a page, or
+  // of half a page for 128-token pages (the bf16 kernel's sub-tiles hold 64 keys)
+  const bool bf16 = t->dtype == PG_BF16;
+  const cuuint64_t esz = bf16 ? 2 : 1;
   cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1],
                         (cuuint64_t)t->shape[0]};
-  cuuint64_t strides[3] = {(cuuint64_t)t->stride[2], (cuuint64_t)t->stride[1], (cuuint64_t)t->stride[0]};
-  cuuint32_t box[4] = {128, 1, (cuuint32_t)P, 1};
+  cuuint64_t strides[3] = {(cuuint64_t)t->stride[2] * esz, (cuuint64_t)t->stride[1] * esz,
+                           (cuuint64_t)t->stride[0] * esz};
+  cuuint32_t box[4] = {bf16 ? 64u : 128u, 1, (cuuint32_t)(bf16 && P > 64 ? 64 : P), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, t->data, dims, strides, box, estr,
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, t->data, dims,
+                  strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {

@@ -51,16 +51,56 @@ SMALL_CASES = [
 ]
 
 
+def _assert_tcgen05_only(path):
+    """Under the automatic path every class ran on a tcgen05 kernel (path bits 2 / 4), never on
+    the warp-MMA kernel (8 / 16)."""
+    import paged_gqa_gb300 as pg
+    if path == "auto":
+        bits = pg.paged_gqa_last_plan()["path_bits"]
+        assert bits & 6 and not bits & 24, f"path bits {bits}"
+
+
 @pytest.mark.parametrize("i", range(len(SMALL_CASES)))
 def test_small_cases_match_oracle(i, path):
     case = _small(1000 + i, **SMALL_CASES[i])
     got = gu.run_library(case)
+    _assert_tcgen05_only(path)
     gu.check_full(case, got, f"case {i} path {path}")
+
+
+BF16_CASES = [
+    # bf16 q and caches (the tcgen05 bf16 kernel serves both classes): verify blocks of
+    # several G on every page size, prefill blocks with a ragged last block and a cached
+    # prefix, both classes in one call, a long sequence split across CTAs
+    dict(group=16, num_kv_heads=1, page_size=32, q_lens=[4, 1, 3], max_ctx=2000),
+    dict(group=8, num_kv_heads=2, page_size=128, q_lens=[2, 8, 5], max_ctx=1700),
+    dict(group=3, num_kv_heads=4, page_size=64, q_lens=[1, 4], max_ctx=300),
+    dict(group=8, num_kv_heads=1, page_size=16, q_lens=[300, 17, 4], max_ctx=1200),
+    dict(group=12, num_kv_heads=2, page_size=128, q_lens=[100, 33], max_ctx=900),
+    dict(group=32, num_kv_heads=1, page_size=64, q_lens=[1, 2, 3, 4], max_ctx=1300),
+]
+
+
+@pytest.mark.parametrize("i", range(len(BF16_CASES)))
+def test_bf16_cache_cases_match_oracle(i, path):
+    case = _small(1100 + i, kv_dtype="bf16", **BF16_CASES[i])
+    got = gu.run_library(case)
+    _assert_tcgen05_only(path)
+    gu.check_full(case, got, f"bf16 case {i} path {path}")
+
+
+def test_bf16_long_sequence_is_split(path):
+    spec = wl.CaseSpec("long bf16", [(4, 30000)], 16, 1, 16, kv_dtype="bf16")
+    case = wl.make_case(spec, device="cuda", seed=14, poison=True)
+    got = gu.run_library(case)
+    _assert_tcgen05_only(path)
+    gu.check_full(case, got, "long split bf16")
 
 
 def test_config1_tiny_verify(path):
     case = wl.make_case(wl.config_spec(1), device="cuda", seed=0, poison=True)
     got = gu.run_library(case)
+    _assert_tcgen05_only(path)
     gu.check_full(case, got, "config 1")
 
 
