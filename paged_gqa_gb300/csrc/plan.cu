@@ -19,11 +19,11 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 
-// Block-wide exclusive scan of one value per thread (1024 threads). Returns the
-// exclusive prefix; *total receives the sum.
+// Block-wide exclusive scan of one value per thread (any multiple of 32 threads up to 1024).
+// Returns the exclusive prefix; *total receives the sum.
 __device__ long long block_exclusive_scan(long long v, long long* total) {
   __shared__ long long warp_sums[32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   long long x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -33,7 +33,7 @@ __device__ long long block_exclusive_scan(long long v, long long* total) {
   if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    long long w = warp_sums[lane];
+    long long w = lane < nwarps ? warp_sums[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       long long y = __shfl_up_sync(0xffffffffu, w, o);
@@ -365,7 +365,13 @@ cudaError_t launch_plan(const Problem& p, const Pointers& ptr, const ClassPlan& 
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = 1;
   }
-  plan_kernel<<<1, kPlanThreads, kPlanSmem, stream>>>(p, ptr, v, f);
+  // A small problem (up to 256 sequences and row blocks per class, 256 CTAs) is planned by
+  // 256 threads: the plan is a chain of block-wide scans, and each barrier over 8 warps is
+  // cheaper than over 32. Larger problems take 1024 threads.
+  const long long rows = (long long)p.T * p.G;
+  const long long blocks = (long long)p.Hkv * ((rows + kPrefillRows - 1) / kPrefillRows + p.num_seqs);
+  const int threads = (p.num_seqs <= 256 && blocks <= 256 && v.num_ctas <= 255 && f.num_ctas <= 255) ? 256 : kPlanThreads;
+  plan_kernel<<<1, threads, kPlanSmem, stream>>>(p, ptr, v, f);
   return cudaGetLastError();
 }
 
