@@ -74,6 +74,8 @@ def parse():
                     help="target CPU time of the oracle sample of each extra workload")
     ap.add_argument("--no-extra-configs", action="store_true",
                     help="time only --config (by default the MTP verify line also times workloads 1, 3, 4, 5)")
+    ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2],
+                    help="kernel path (paged_gqa_set_path): 0 auto, 1 warp-level MMA, 2 auto + tcgen05 sparse kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -335,6 +337,7 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pg.load()
+    pg.paged_gqa_set_path(args.path)
     spec = attn_spec(args)
     case = wl.make_case(spec, device=dev, seed=rank)  # each rank: an independent replica
     T, Hq = case.q.shape[0], case.q.shape[1]
@@ -461,6 +464,7 @@ def run_cache_write(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pg.load()
+    pg.paged_gqa_set_path(args.path)
     spec = _cw_spec(args)
     case = wl.make_case(spec, device=dev, seed=rank)
     kn, vn = _new_tokens(spec, dev, rank)
@@ -641,6 +645,7 @@ def run_sparse(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pg.load()
+    pg.paged_gqa_set_path(args.path)
     spec = wl.sparse_spec(args.sparse_tp)
     case = wl.make_case(spec, device=dev, seed=rank)
     idx = wl.sparse_indices(spec, wl.SPARSE_TOPK, device=dev, seed=rank)
@@ -712,10 +717,12 @@ def run_sparse(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "us_per_call": round(step_ms * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16 (e4m3 K/V, bf16 q)",
         "data": "synthetic (seeded N(0,1) Q/K/V, FP8 per-tensor amax/448; stratified random top-k lists)",
-        "config": sp_config(spec, args.sparse_tp, world, "flushed: 512 MiB memset between timed calls", used),
+        "config": dict(sp_config(spec, args.sparse_tp, world, "flushed: 512 MiB memset between timed calls", used),
+                       kernel_path=args.path),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16, "unit": "TFLOP/s",
                      "frac": round(achieved / bf16, 4), "peak_source": f"{peak_src} (bf16_tflops burst; f16 dense = bf16)",
-                     "kernel": "sparse", "kernel_us": round(step_ms * 1e3, 2),
+                     "kernel": "sparse_tc" if pg.paged_gqa_last_plan()["path_bits"] & 32 else "sparse",
+                     "kernel_us": round(step_ms * 1e3, 2),
                      "gathered_GBps": round(used // spec.group * 512 / 1e9 / (step_ms / 1e3), 1),
                      "traffic": None},
         "gpu_launches": K, "clocks": clocks, "wall_s": round(wall, 3),
