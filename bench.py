@@ -724,7 +724,8 @@ def run_sparse(args, rank, world, local):
                      "kernel": "sparse_tc" if pg.paged_gqa_last_plan()["path_bits"] & 32 else "sparse",
                      "kernel_us": round(step_ms * 1e3, 2),
                      "gathered_GBps": round(used // spec.group * 512 / 1e9 / (step_ms / 1e3), 1),
-                     "traffic": None},
+                     "traffic": traffic_for("sparse_tc" if pg.paged_gqa_last_plan()["path_bits"] & 32 else "sparse",
+                                            spec.name)},
         "gpu_launches": K, "clocks": clocks, "wall_s": round(wall, 3),
     }
     if e2e:
