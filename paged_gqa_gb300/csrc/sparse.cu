@@ -5,10 +5,11 @@
 // The tile of one unit (token t, kv head h, up to 16 of its query heads) has M = 16 rows,
 // too few for a tcgen05 tile: the products run on warp-level mma.sync m16n8k16 (f16 in,
 // fp32 accumulate). e4m3 K/V convert to f16 exactly; bf16 Q is converted to f16 once,
-// after scaling the unit's Q by a power of two 2^sig that puts its largest |q| in
-// [2^14, 2^15): every bf16 value within 2^-24 of that maximum is then exact in f16 (bf16
-// values beyond f16's range, or below its normal range, included), and 2^-sig goes into
-// the score scale.
+// after each warp scales its half of the unit's Q (its 128 dims) by a power of two 2^sig
+// that puts that half's largest |q| in [2^14, 2^15): every bf16 value within 2^-24 of that
+// maximum is then exact in f16 (bf16 values beyond f16's range, or below its normal range,
+// included), and the warp multiplies its partial scores by 2^-sig (exact) before the pair
+// adds them.
 //
 // Work split: a pair of warps per unit; warp w owns head dims [128w, 128w + 128). Per step
 // of 16 listed keys each warp computes the partial S of all 16 keys over its d-half (two
@@ -44,7 +45,6 @@ constexpr float kTauSp = 8.f;             // p <= 2^8 between rescales (f16 hold
 
 struct alignas(16) PairSmem {
   float xs[2][2][32][8];  // [step parity][warp][lane]: the warp's partial S fragment (2 n8 tiles)
-  float qmax[4];          // [warp]: max |q| over the warp's d-half of the unit's rows
 };
 // xs is read and written as float4: every pair's copy must start on 16 bytes
 static_assert(sizeof(PairSmem) % 16 == 0, "PairSmem array elements stay 16-byte aligned");
@@ -148,15 +148,13 @@ __global__ void __launch_bounds__(kSpThreads, 3) sparse_attn_kernel(SparseArgs a
 #pragma unroll
       for (int k = 0; k < 4; ++k) qmax = fmaxf(qmax, bf16x2_absmax(word_of(raw[half][i], k)));
   }
-  // the unit's max |q| (both warps of the pair), then 2^sig with 2^sig * max in [2^14, 2^15)
+  // max |q| over this warp's d-half of the unit's rows, then 2^sig with 2^sig * max in
+  // [2^14, 2^15)
   qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
   qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
   qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 4));
   qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 8));
   qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 16));
-  if (lane == 0) ps.qmax[w] = qmax;
-  pair_sync(pair);
-  qmax = fmaxf(ps.qmax[0], ps.qmax[1]);
   int sig = 0;
   if (qmax > 0.f && qmax <= 3.0e38f) sig = 14 - ((int)((__float_as_uint(qmax) >> 23) & 0xff) - 127);
   sig = max(-120, min(120, sig));
@@ -177,7 +175,8 @@ __global__ void __launch_bounds__(kSpThreads, 3) sparse_attn_kernel(SparseArgs a
   for (int m = 0; m < 16; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
   float m_ref[2] = {-INFINITY, -INFINITY};  // rows g, g+8 (the same in both warps)
   float l_row[2] = {0.f, 0.f};             // this thread's keys' share of the row sums
-  const float c = a.score_scale_log2 * ldexpf(1.f, -sig);  // scores of the unscaled q
+  const float c = a.score_scale_log2;
+  const float unscale = ldexpf(1.f, -sig);  // this warp's partial scores back to the unscaled q
 
   const int32_t* list = a.idx + (long long)t * a.idx_st + (long long)kvh * a.idx_sh;
   const int K = unit_ok ? a.K : 0;
@@ -248,7 +247,12 @@ __global__ void __launch_bounds__(kSpThreads, 3) sparse_attn_kernel(SparseArgs a
                   e4m3x2_f16x2(kw >> 16));
         }
       }
-      // the pair's halves add up to the full S (a + b = b + a: both warps get the same bits)
+      // the pair's halves add up to the full S (a + b = b + a: both warps get the same bits),
+      // each half first scaled back by its warp's exact power of two
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sp[j][i] *= unscale;
       float4* mine = reinterpret_cast<float4*>(&ps.xs[par][w][lane][0]);
       mine[0] = make_float4(sp[0][0], sp[0][1], sp[0][2], sp[0][3]);
       mine[1] = make_float4(sp[1][0], sp[1][1], sp[1][2], sp[1][3]);
