@@ -55,6 +55,23 @@ METRIC = "us/call and KV-read GB/s (verify) / TFLOP/s (prefill) as % of GB300 ro
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
+L2_NOTE = "flushed: 512 MiB memset, then a 512 MiB read, between timed calls (no input line and no dirty line left in L2)"
+
+
+class L2Flush:
+    """Between timed calls: write a buffer four times the L2 (evicts every input line), then
+    read another as large, so the memset's dirty lines are written back here and not inside
+    the next timed call (a memset alone left ~130 MB of dirty lines whose write-back cost the
+    MTP verify call ~4.5 us and workload 3 ~12 us)."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.acc = torch.zeros((), dtype=torch.int64, device=dev)
+
+    def zero_(self):
+        self.w.zero_()
+        torch.sum(self.r, 0, dtype=torch.int64, out=self.acc)
 
 
 def parse():
@@ -74,8 +91,9 @@ def parse():
                     help="target CPU time of the oracle sample of each extra workload")
     ap.add_argument("--no-extra-configs", action="store_true",
                     help="time only --config (by default the MTP verify line also times workloads 1, 3, 4, 5)")
-    ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2],
-                    help="kernel path (paged_gqa_set_path): 0 auto, 1 warp-level MMA, 2 auto + tcgen05 sparse kernel")
+    ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="kernel path (paged_gqa_set_path): 0 auto, 1 warp-level MMA, 2 auto + tcgen05 sparse "
+                         "kernel, 3 auto with the verify class planned by the plan kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -342,7 +360,7 @@ def run_ours(args, rank, world, local):
     case = wl.make_case(spec, device=dev, seed=rank)  # each rank: an independent replica
     T, Hq = case.q.shape[0], case.q.shape[1]
     out = torch.empty(T, Hq, wl.HEAD_DIM, dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     kind, dominant_cls = _dominant(spec, args.config)
 
     quant_q = args.op == "attn_quant_q"
@@ -413,7 +431,7 @@ def run_ours(args, rank, world, local):
         "us_per_call": round(step_ms * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if kernel_kind != "portable" else "tf32",
         "data": "synthetic (seeded N(0,1), FP8 per-tensor amax/448)",
-        "config": config_dict(spec, args.config, world, "flushed: 512 MiB memset between timed calls", quant_q),
+        "config": config_dict(spec, args.config, world, L2_NOTE, quant_q),
         "roofline": _roofline(spec, kind, kern_avg_ms, kernel_kind),
         "gpu_launches": int(plan["kernels_launched"]) * K,
         "clocks": clocks,
@@ -468,7 +486,7 @@ def run_cache_write(args, rank, world, local):
     spec = _cw_spec(args)
     case = wl.make_case(spec, device=dev, seed=rank)
     kn, vn = _new_tokens(spec, dev, rank)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     bytes_per_step = spec.total_q * spec.num_kv_heads * CW_ROW_BYTES
 
     def call(k_new=kn, v_new=vn, bt=case.block_table, sl=case.seq_lens, qsl=case.query_start_loc):
@@ -535,7 +553,7 @@ def run_cache_write(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "us_per_call": round(step_ms * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3",
         "data": "synthetic (seeded N(0,1) new K/V; the config's paged cache and block table)",
-        "config": cw_config(spec, args.config, world, "flushed: 512 MiB memset between timed calls"),
+        "config": cw_config(spec, args.config, world, L2_NOTE),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "peak_source": f"{peak_src} (hbm_gbs)",
                      "kernel": "cache_write", "kernel_us": round(step_ms * 1e3, 2),
@@ -652,7 +670,7 @@ def run_sparse(args, rank, world, local):
     used = sp_used_pairs(spec, idx)
     flops = used * 4 * wl.HEAD_DIM
     out = torch.empty(case.q.shape[0], case.q.shape[1], wl.HEAD_DIM, dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def call(q=case.q, ix=idx, bt=case.block_table, sl=case.seq_lens, qsl=case.query_start_loc):
         pg.paged_gqa_sparse_attn(q, case.k_cache, case.v_cache, bt, sl, qsl, ix, case.k_descale,
@@ -717,7 +735,7 @@ def run_sparse(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "us_per_call": round(step_ms * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16 (e4m3 K/V, bf16 q)",
         "data": "synthetic (seeded N(0,1) Q/K/V, FP8 per-tensor amax/448; stratified random top-k lists)",
-        "config": dict(sp_config(spec, args.sparse_tp, world, "flushed: 512 MiB memset between timed calls", used),
+        "config": dict(sp_config(spec, args.sparse_tp, world, L2_NOTE, used),
                        kernel_path=args.path),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16, "unit": "TFLOP/s",
                      "frac": round(achieved / bf16, 4), "peak_source": f"{peak_src} (bf16_tflops burst; f16 dense = bf16)",

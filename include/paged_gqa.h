@@ -118,7 +118,10 @@ int paged_gqa_attn(const pg_tensor* q, const pg_tensor* k_cache, const pg_tensor
  * paged_gqa_attn_ex -- the same call with an explicit q descale (multiplied into
  * softmax_scale) and a caller-owned device workspace of at least
  * paged_gqa_workspace_size(...) bytes, 256-byte aligned. Allocates nothing.
- * The workspace must not be shared by calls that can overlap on the device.
+ * The workspace must not be shared by calls that can overlap on the device. Its contents
+ * need no initialisation and may be left from any earlier use: the split-KV merge
+ * counters in it carry a 48-bit per-call tag (a counter word that holds this call's tag
+ * by chance, about 2^-48 per split block, would mistime that block's merge).
  */
 int paged_gqa_attn_ex(const pg_tensor* q, const pg_tensor* k_cache, const pg_tensor* v_cache,
                       const pg_tensor* block_table, const pg_tensor* seq_lens,
@@ -253,6 +256,9 @@ int paged_gqa_check_device_errors(pg_stream_t stream);
  *       faster of the two on the sparse workloads)
  *   1 = warp-level MMA (mma.sync) kernel for every tile
  *   2 = as 0, but sparse calls with lists of 64 or more entries use the tcgen05 kernel
+ *   3 = as 0, but the verify class is always planned by the plan kernel before its
+ *       kernel runs (under 0 the tcgen05 verify kernel plans it itself when
+ *       num_seqs x num_kv_heads <= 512; results are identical)
  * Returns the previous value, or PG_ERR_INVALID_ARG.
  */
 int paged_gqa_set_path(int path);
@@ -275,8 +281,8 @@ int paged_gqa_set_stall_test(uint32_t wait_ns);
  * tests and the benchmark. out8 receives {verify CTAs, prefill CTAs, kernels
  * launched, path bits (2: tcgen05 verify, 4: tcgen05 prefill, 8: warp-MMA verify,
  * 16: warp-MMA prefill, 32: tcgen05 sparse, 64: warp-MMA sparse), verify block bound,
- * prefill block bound, workspace bytes, 0}. A sparse call sets only the launch count and
- * the path bits.
+ * prefill block bound, workspace bytes, 1 if the verify kernel planned its own class}.
+ * A sparse call sets only the launch count and the path bits.
  */
 int paged_gqa_last_plan(int64_t* out8);
 

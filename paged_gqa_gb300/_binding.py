@@ -239,7 +239,7 @@ def paged_gqa_last_plan() -> dict:
     buf = (ctypes.c_int64 * 8)()
     _check(load().paged_gqa_last_plan(buf))
     keys = ("verify_ctas", "prefill_ctas", "kernels_launched", "path_bits", "max_verify_blocks",
-            "max_prefill_blocks", "workspace_bytes", "reserved")
+            "max_prefill_blocks", "workspace_bytes", "verify_self_planned")
     return dict(zip(keys, list(buf)))
 
 

@@ -34,6 +34,14 @@ thread_local std::string t_last_error;
 thread_local int64_t t_last_plan[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 std::atomic<int> g_path{0};
 std::atomic<uint32_t> g_stall_test_ns{0};
+std::atomic<uint32_t> g_call_seq{0};
+
+// Nonzero, new on every call (Problem::call_tag).
+uint32_t next_call_tag() {
+  uint32_t t;
+  do t = g_call_seq.fetch_add(1) + 1; while (t == 0);
+  return t;
+}
 std::atomic<cudaEvent_t> g_ev_start[kNumClasses], g_ev_stop[kNumClasses];
 
 int fail(int code, const char* fmt, ...) {
@@ -120,6 +128,7 @@ struct WsLayout {
   ClassSizes cls[kNumClasses];
   size_t off[kNumClasses][8];
   size_t q_amax_off;  // per-CTA maxima of |q| (calls that quantise Q)
+  size_t epoch_off;   // the split counters' epoch word
   size_t total;
 };
 
@@ -140,16 +149,15 @@ WsLayout make_layout(int num_seqs, int T, int Hq, int Hkv, int sms) {
     s.num_ctas = sms;
     s.max_blocks = (int)std::max<long long>(1, nb[c]);
     s.max_items = s.max_blocks + s.num_ctas;
-    // Split pieces: at most two per CTA range, and at most one per block plus one per
-    // CTA boundary that falls inside a block.
-    s.max_slots = nb[c] == 0 ? 0 : (int)std::min<long long>(2LL * s.num_ctas, nb[c] + s.num_ctas - 1);
+    // Split pieces take slots by split_slot_base: below 2 per CTA.
+    s.max_slots = nb[c] == 0 ? 0 : 2 * s.num_ctas;
     s.slot_rows = rows[c];
     size_t sz[8] = {
         256,                                                          // n_blocks, n_items, total_tiles
         sizeof(int) * (size_t)(s.num_ctas + 1),                       // cta_item_begin
         sizeof(RowBlock) * (size_t)s.max_blocks,                      // blocks
         sizeof(WorkItem) * (size_t)s.max_items,                       // items
-        sizeof(int) * (size_t)s.max_blocks,                           // counters
+        sizeof(unsigned long long) * (size_t)s.max_blocks,            // counters
         sizeof(uint16_t) * (size_t)s.max_slots * s.slot_rows * kHeadDim, // part_o (f16)
         sizeof(float) * (size_t)s.max_slots * s.slot_rows,            // part_lse
         0};
@@ -160,6 +168,8 @@ WsLayout make_layout(int num_seqs, int T, int Hq, int Hkv, int sms) {
   }
   L.q_amax_off = at;
   at += align256(sizeof(float) * (size_t)q_amax_parts(sms));
+  L.epoch_off = at;
+  at += 256;
   L.total = at;
   return L;
 }
@@ -173,7 +183,8 @@ ClassPlan class_plan(const WsLayout& L, int c, char* base) {
   cp.cta_item_begin = reinterpret_cast<int*>(base + o[1]);
   cp.blocks = reinterpret_cast<RowBlock*>(base + o[2]);
   cp.items = reinterpret_cast<WorkItem*>(base + o[3]);
-  cp.counters = reinterpret_cast<int*>(base + o[4]);
+  cp.counters = reinterpret_cast<unsigned long long*>(base + o[4]);
+  cp.epoch = reinterpret_cast<unsigned long long*>(base + L.epoch_off);
   cp.part_o = reinterpret_cast<uint16_t*>(base + o[5]);
   cp.part_lse = reinterpret_cast<float*>(base + o[6]);
   cp.num_ctas = L.cls[c].num_ctas;
@@ -324,21 +335,40 @@ int run(const Validated& val, const pg_tensor* k, const pg_tensor* v, void* ws, 
     if (e != cudaSuccess) return cuda_fail(e, "q amax launch");
     ++launched;
   }
-  e = launch_plan(p, ptr, cp[0], cp[1], stream);
-  if (e != cudaSuccess) return cuda_fail(e, "plan launch");
-  ++launched;
+  p.call_tag = next_call_tag();
+  // The verify kernel plans its own class when its CTAs can hold one entry per verify block
+  // (sequence x kv head), the class's units fit 31 bits and a block's tiles 16: it then runs
+  // first, and the plan kernel (prefill only) and the prefill kernel follow it as
+  // programmatic dependents, off the critical path.
+  const long long max_tiles = ((long long)p.W * p.P + kTileKeys - 1) / kTileKeys;
+  p.fused_verify = fast_ok && path != 3 && (long long)p.num_seqs * p.Hkv <= kFusedMaxBlocks &&
+                   max_tiles < (1 << 16) &&
+                   (long long)p.num_seqs * p.Hkv * (max_tiles + fixed_cost(0)) < (1LL << 31);
+  if (!p.fused_verify) {
+    e = launch_plan(p, ptr, cp[0], cp[1], true, false, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+    ++launched;
+  }
   int used = 0;
   bool prev_ev = false;  // an event was recorded after the previous class's kernel
   for (int c = 0; c < kNumClasses; ++c) {
     bool done = false;
     cudaEvent_t ev0 = g_ev_start[c].load(), ev1 = g_ev_stop[c].load();
+    bool after_plan = false;  // this class's kernel directly follows the plan kernel
+    if (c == 1 && p.fused_verify) {
+      e = launch_plan(p, ptr, cp[0], cp[1], false, !prev_ev, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+      ++launched;
+      after_plan = true;
+    }
     if (ev0 && (e = cudaEventRecord(ev0, stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     if (fast_ok || bf16_ok) {
-      // the prefill-class kernel follows the verify-class one as a programmatic dependent
-      // (when that one is a tcgen05 kernel too and no event sits between them)
-      const bool dependent = c == 1 && (used & 2) && !ev0 && !prev_ev;
+      // the prefill-class kernel follows the verify-class one (or the plan kernel, when the
+      // verify kernel planned itself) as a programmatic dependent, when that one is a
+      // tcgen05 kernel too and no event sits between them
+      const bool dependent = c == 1 && !ev0 && (after_plan || ((used & 2) && !prev_ev));
       int r = bf16_ok ? launch_bf16_tc(p, ptr, cp[c], k, v, stream, dependent)
-              : (c == 0) ? launch_verify_tc(p, ptr, cp[c], k, v, ds->sms, stream)
+              : (c == 0) ? launch_verify_tc(p, ptr, cp[c], k, v, ds->sms, stream, !p.fused_verify && pdl_enabled())
                          : launch_prefill_tc(p, ptr, cp[c], k, v, ds->sms, stream, dependent);
       if (r < 0) return fail(PG_ERR_CUDA, "tcgen05 %s launch failed: %s", c == 0 ? "verify" : "prefill",
                              tc_last_error());
@@ -364,6 +394,7 @@ int run(const Validated& val, const pg_tensor* k, const pg_tensor* v, void* ws, 
   plan_info[4] = cp[0].max_blocks;
   plan_info[5] = cp[1].max_blocks;
   plan_info[6] = (int64_t)L.total;
+  plan_info[7] = p.fused_verify;
   memcpy(t_last_plan, plan_info, sizeof plan_info);
   return PG_OK;
 }
@@ -407,6 +438,10 @@ int attn_common(const pg_tensor* q, const pg_tensor* k, const pg_tensor* v, cons
       size_t want = L.total + L.total / 4;
       e = cudaMalloc(&ds->ws, want);
       if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+      // not required (the split counters are tagged per call), but keeps the first call's
+      // workspace contents deterministic
+      e = cudaMemsetAsync(ds->ws, 0, want, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace)");
       ds->ws_bytes = want;
     }
     st = run(val, k, v, ds->ws, ds->ws_bytes, L, ds, stream);
@@ -577,7 +612,7 @@ int paged_gqa_check_device_errors(pg_stream_t stream) {
 }
 
 int paged_gqa_set_path(int path) {
-  if (path < 0 || path > 2) return fail(PG_ERR_INVALID_ARG, "path must be 0, 1 or 2");
+  if (path < 0 || path > 3) return fail(PG_ERR_INVALID_ARG, "path must be 0, 1, 2 or 3");
   return g_path.exchange(path);
 }
 

@@ -91,6 +91,29 @@ __device__ __forceinline__ int seq_of_token(const int32_t* qsl, int n, int t, in
 
 constexpr int kMergeMaxSplits = 16;  // pieces whose weights fit the shared scratch
 
+// This call's 48-bit tag for the split counters: the workspace's epoch word (advanced by
+// the plan kernel once per call, after every kernel of the call that reads it has read it)
+// mixed with the host's nonzero per-call value. A constant fill of the workspace never
+// carries it (the mix of a nonzero value with an odd constant is nonzero below bit 48), and
+// leftover bytes of other data carry it with probability 2^-48 per counter.
+__device__ __forceinline__ unsigned long long split_tag(const Problem& p, const ClassPlan& cp) {
+  return (__ldcg(cp.epoch) ^ ((unsigned long long)p.call_tag * 0x9E3779B97F4A7C15ull)) & kSplitTagMask;
+}
+
+// One piece of a split block has stored its partial; true for the block's last piece. The
+// counter word holds (tag << 16) | arrivals (nsplit < 2^16); a word with another tag counts
+// as no arrivals. The CAS loop retries only while other pieces of the block arrive.
+__device__ __forceinline__ bool split_arrive(unsigned long long* counter, int nsplit, unsigned long long tag) {
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(counter);
+  for (;;) {
+    const unsigned arrived = (old >> 16) == tag ? (unsigned)(old & 0xffffu) : 0u;
+    const unsigned long long want = (tag << 16) | (arrived + 1u);
+    const unsigned long long seen = atomicCAS(counter, old, want);
+    if (seen == old) return arrived + 1u == (unsigned)nsplit;
+    old = seen;
+  }
+}
+
 // Called by `nthreads` threads (ids tid = 0..nthreads-1) that share barrier `bar_id`,
 // after each has written its share of this piece's partial result (normalised O in f16
 // code units and log2-sum-exp per row) and executed __threadfence(). The last piece of a
@@ -106,8 +129,7 @@ __device__ inline void finish_split_block(const Problem& p, const Pointers& ptr,
   named_barrier(bar_id, nthreads);
   if (tid == 0) {
     __threadfence();
-    int old = atomicAdd(&cp.counters[block_index], 1);
-    *s_flag = (old == rb.nsplit - 1);
+    *s_flag = split_arrive(cp.counters + block_index, rb.nsplit, split_tag(p, cp));
     __threadfence();
   }
   named_barrier(bar_id, nthreads);

@@ -14,9 +14,9 @@
 //   * a call whose workspace need (paged_gqa_workspace_size) exceeds it returns
 //     PG_ERR_WORKSPACE with a message stating both sizes, and launches nothing;
 //   * every call on a device uses the same array, which keeps whatever the last call left
-//     there. Each call clears what must start at zero (its merge counters) before use,
-//     so results never depend on earlier calls, but two calls whose work can overlap on
-//     the GPU (different streams without ordering between them) race on the array: order
+//     there. The merge counters in it carry a per-call tag (nothing needs clearing), so
+//     results do not depend on earlier calls, but two calls whose work can overlap on the
+//     GPU (different streams without ordering between them) race on the array: order
 //     them on one stream, or use paged_gqa_attn_ex with separate workspaces;
 //   * the first call on each device looks up the array's device address
 //     (cudaGetSymbolAddress) with that device current; make that first call before any

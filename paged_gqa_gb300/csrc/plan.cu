@@ -12,6 +12,7 @@
 
 #include "common.cuh"
 #include "plan.cuh"
+#include "tc_kernels.cuh"
 
 namespace pgqa {
 
@@ -72,15 +73,6 @@ __device__ int blocks_per_head(const SeqInfo& si, int G, int cls) {
   return verify ? 0 : (int)((rows + kPrefillRows - 1) / kPrefillRows);
 }
 
-// CTA that owns unit u when U units are cut into C ranges [floor(c*U/C), floor((c+1)*U/C)).
-__device__ __forceinline__ int cta_of(long long u, long long U, int C) {
-  return (int)(((u + 1) * C + U - 1) / U) - 1;
-}
-
-__device__ __forceinline__ long long range_begin(int c, long long U, int C) {
-  return (long long)c * U / C;
-}
-
 }  // namespace
 
 // Shared-memory caches: sequence info, per-sequence block prefixes and per-block tile
@@ -90,9 +82,8 @@ __device__ __forceinline__ long long range_begin(int c, long long U, int C) {
 constexpr int kSeqCache = 2048;
 constexpr int kBlockCache = 12288;
 constexpr int kMaxCtas = 1024;
-// What starting a row block costs a CTA, in key tiles (Q load, epilogue, merge): measured
+// fixed_cost(cls) (common.cuh), what starting a row block costs a CTA in key tiles: measured
 // about 8 us at ~1.6 us per tile for verify blocks; prefill blocks have longer tiles.
-__host__ __device__ constexpr int fixed_cost(int cls) { return cls == 0 ? 5 : 2; }
 constexpr size_t kPlanSmem = sizeof(int4) * kSeqCache + sizeof(int) * (kSeqCache + 1) +
                              sizeof(long long) * kBlockCache + sizeof(int) * kBlockCache +
                              sizeof(int) * (kMaxCtas + 1);
@@ -216,33 +207,25 @@ __device__ __forceinline__ void plan_class(const Problem& p, const Pointers& ptr
   }
   const long long U = tbase;
   // At most U ranges, none empty in units (a range may hold no tile: that CTA has no item).
-  const int C = (int)min((long long)cp.num_ctas, U);
+  const int C = cut_ctas(U, cp.num_ctas);
 
-  // ---- per-block split count and partial slots; block containing the start of each range
-  int slot_base = 0;
-  for (int b0 = 0; b0 < nblocks; b0 += blockDim.x) {
-    const int b = b0 + threadIdx.x;
-    int ns = 0;
-    if (b < nblocks) {
-      const long long span = off_of(b), real = span + E;  // tiles occupy [real, real + tiles)
-      const int tiles = tiles_of(b);
-      ns = cta_of(real + tiles - 1, U, C) - cta_of(real, U, C) + 1;  // pieces: ranges meeting the tiles
-      cp.counters[b] = 0;
-      // CTA c's range starts inside block b's span for c in (c_first, c_last], and at its
-      // first unit when the range boundary falls exactly there
-      const int c_first = cta_of(span, U, C), c_last = cta_of(span + E + tiles - 1, U, C);
-      if (range_begin(c_first, U, C) == span) sm.bfirst[c_first] = b;
-      for (int c = c_first + 1; c <= c_last; ++c) sm.bfirst[c] = b;
-    }
-    const int nslots = ns > 1 ? ns : 0;
-    const long long pre = block_exclusive_scan(nslots, sm.total) + slot_base;
-    if (b < nblocks) {
-      *reinterpret_cast<int2*>(reinterpret_cast<int*>(cp.blocks + b) + 8) = make_int2(ns, (int)pre);
-      if (nslots > 0 && pre + nslots > cp.max_slots) *sm.overflow = 1;
-    }
-    slot_base += (int)*sm.total;
-    __syncthreads();
+  // ---- per-block split count and partial slots (split_slot_base: no scan); block containing
+  // the start of each range
+  for (int b = threadIdx.x; b < nblocks; b += blockDim.x) {
+    const long long span = off_of(b), real = span + E;  // tiles occupy [real, real + tiles)
+    const int tiles = tiles_of(b);
+    const int c0 = cta_of(real, U, C);
+    const int ns = cta_of(real + tiles - 1, U, C) - c0 + 1;  // pieces: ranges meeting the tiles
+    const int slot = split_slot_base(c0, range_begin(c0, U, C) < span);
+    *reinterpret_cast<int2*>(reinterpret_cast<int*>(cp.blocks + b) + 8) = make_int2(ns, slot);
+    if (ns > 1 && slot + ns > cp.max_slots) *sm.overflow = 1;
+    // CTA c's range starts inside block b's span for c in (c_first, c_last], and at its
+    // first unit when the range boundary falls exactly there
+    const int c_first = cta_of(span, U, C), c_last = cta_of(span + E + tiles - 1, U, C);
+    if (range_begin(c_first, U, C) == span) sm.bfirst[c_first] = b;
+    for (int c = c_first + 1; c <= c_last; ++c) sm.bfirst[c] = b;
   }
+  __syncthreads();
 
   // ---- items: count per CTA, scan, fill. The items of range [u0, u1) are the blocks whose
   // tiles meet it: from the block whose span holds u0 to the block whose span holds
@@ -303,8 +286,11 @@ __device__ __forceinline__ void empty_class(const ClassPlan& cp) {
   }
 }
 
+// With plan_verify false the verify class is planned by its own kernel (Problem::fused_verify),
+// which runs first: this kernel then plans prefill only, and advances the epoch word once
+// that kernel has completed.
 __global__ void __launch_bounds__(kPlanThreads, 1)
-plan_kernel(Problem p, Pointers ptr, ClassPlan c0, ClassPlan c1) {
+plan_kernel(Problem p, Pointers ptr, ClassPlan c0, ClassPlan c1, int plan_verify) {
   __shared__ long long s_total;
   __shared__ int s_overflow;
   extern __shared__ __align__(16) unsigned char plan_smem[];
@@ -340,22 +326,31 @@ plan_kernel(Problem p, Pointers ptr, ClassPlan c0, ClassPlan c1) {
           for (int d = 0; d < kHeadDim; ++d) o[t * p.o_st + h * p.o_sh + d] = 0;
     }
   }
-  has_v = __syncthreads_or(has_v);
+  has_v = __syncthreads_or(has_v) && plan_verify;
   has_p = __syncthreads_or(has_p);
-  if (has_v) plan_class(p, ptr, c0, 0, sm); else empty_class(c0);
+  if (plan_verify) {
+    if (has_v) plan_class(p, ptr, c0, 0, sm); else empty_class(c0);
+  }
   if (has_p) plan_class(p, ptr, c1, 1, sm); else empty_class(c1);
   if (threadIdx.x == 0 && s_overflow) {
     // Host-side bounds make this unreachable; flag it rather than run a partial plan.
     atomicOr(ptr.err, kErrBounds);
-    *c0.n_items = 0;
+    if (plan_verify) {
+      *c0.n_items = 0;
+      for (int c = 0; c <= c0.num_ctas; ++c) c0.cta_item_begin[c] = 0;
+    }
     *c1.n_items = 0;
-    for (int c = 0; c <= c0.num_ctas; ++c) c0.cta_item_begin[c] = 0;
     for (int c = 0; c <= c1.num_ctas; ++c) c1.cta_item_begin[c] = 0;
   }
+  // New split-counter tag for the next call: every kernel of this call that reads the epoch
+  // word reads it after this grid completes, or (a self-planned verify kernel, which this grid
+  // may follow as a programmatic dependent) has completed before this point.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) *c0.epoch += 1ull;
 }
 
 cudaError_t launch_plan(const Problem& p, const Pointers& ptr, const ClassPlan& v,
-                        const ClassPlan& f, cudaStream_t stream) {
+                        const ClassPlan& f, bool plan_verify, bool dependent, cudaStream_t stream) {
   if (v.num_ctas > kMaxCtas || f.num_ctas > kMaxCtas) return cudaErrorInvalidConfiguration;
   static int attr_done[64] = {0};
   int dev = 0;
@@ -371,8 +366,8 @@ cudaError_t launch_plan(const Problem& p, const Pointers& ptr, const ClassPlan& 
   const long long rows = (long long)p.T * p.G;
   const long long blocks = (long long)p.Hkv * ((rows + kPrefillRows - 1) / kPrefillRows + p.num_seqs);
   const int threads = (p.num_seqs <= 256 && blocks <= 256 && v.num_ctas <= 255 && f.num_ctas <= 255) ? 256 : kPlanThreads;
-  plan_kernel<<<1, threads, kPlanSmem, stream>>>(p, ptr, v, f);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(dependent, plan_kernel, 1, threads, kPlanSmem, stream, p, ptr, v, f, plan_verify ? 1 : 0);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace pgqa

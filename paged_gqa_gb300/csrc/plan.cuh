@@ -4,8 +4,10 @@
 
 namespace pgqa {
 
+// plan_verify false: the verify class plans itself (Problem::fused_verify) and this kernel
+// follows its kernel; dependent: launched as that kernel's programmatic dependent.
 cudaError_t launch_plan(const Problem& p, const Pointers& ptr, const ClassPlan& verify,
-                        const ClassPlan& prefill, cudaStream_t stream);
+                        const ClassPlan& prefill, bool plan_verify, bool dependent, cudaStream_t stream);
 
 // Arguments of the paged KV-cache write (cache_write.cu); strides in elements.
 struct CacheWriteArgs {

@@ -12,8 +12,10 @@
 
 namespace pgqa {
 
+// dependent: launch as a programmatic dependent of the kernel before it on the stream (the
+// plan kernel; off unless pdl_enabled()).
 int launch_verify_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp, const pg_tensor* k,
-                     const pg_tensor* v, int sms, cudaStream_t stream);
+                     const pg_tensor* v, int sms, cudaStream_t stream, bool dependent);
 // dependent: launch as a programmatic dependent of the kernel before it on the stream (the
 // verify-class kernel), so its CTAs are already resident when that kernel ends.
 int launch_prefill_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp, const pg_tensor* k,
@@ -54,7 +56,7 @@ cudaError_t launch_pdl(bool dependent, void (*kernel)(KArgs...), int grid, int b
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = (dependent || pdl_enabled()) ? 1 : 0;
+  cfg.numAttrs = dependent ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 

@@ -123,9 +123,15 @@ struct Misc {
   uint32_t tmem_base;
   int abort_flag;
   int merge_flag;
+  // Self-planned verify class (Problem::fused_verify): this CTA's items, packed by
+  // fused_plan, their count, and the CTA-wide scan's warp totals.
+  int4 fitem[kFusedMaxBlocks];
+  long long scan_warp[kVThreads / 32];
+  int fcount;
 };
 static_assert(offsetof(Misc, m) % 16 == 0 && offsetof(Misc, k_full) % 8 == 0, "Misc alignment");
 constexpr size_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
 
 struct Item {
   int block, seq, kvh, row0, nrows, kv_end, nsplit, split, slot_base;
@@ -133,7 +139,153 @@ struct Item {
   int q0, qn, L;
 };
 
-__device__ __forceinline__ Item load_item(const ClassPlan& cp, const Pointers& ptr, int it) {
+constexpr int kE = fixed_cost(0);
+
+// Self-planned verify class: every CTA works out the plan kernel's cut of the verify blocks
+// (one per verify sequence and kv head, in sequence order, each fixed_cost(0) units and
+// then its ceil(L / 128) key tiles) from query_start_loc and seq_lens, and keeps its own
+// items in shared memory; nothing is written to global memory. The host guarantees
+// num_seqs * Hkv <= kFusedMaxBlocks (so num_seqs < the CTA's threads), U < 2^31 and key
+// tiles per block < 2^16.
+//
+// The cut in 32-bit arithmetic: with U = q C + r, range c starts at floor(c U / C) =
+// c q + floor(c r / C) (c r < 2^20), and the range holding unit u comes from a float
+// estimate of u C / U (off by at most one) and a correction.
+struct Cut {
+  int U, C, q, r;
+};
+__device__ __forceinline__ Cut make_cut(int U, int C) { return Cut{U, C, U / C, U % C}; }
+__device__ __forceinline__ int cut_begin(const Cut& k, int c) {
+  return c * k.q + (int)(((unsigned)c * (unsigned)k.r) / (unsigned)k.C);
+}
+__device__ __forceinline__ int cut_cta(const Cut& k, int u) {
+  int c = (int)((float)u * (float)k.C / (float)k.U);
+  c = min(max(c, 0), k.C - 1);
+  while (c > 0 && cut_begin(k, c) > u) --c;
+  while (c + 1 < k.C && cut_begin(k, c + 1) <= u) ++c;
+  return c;
+}
+
+// Scratch of the self-planned prologue, in the K stages (no copy has touched them yet).
+struct FusedScratch {
+  long long v[kFusedMaxBlocks];  // per sequence: (units << 16) | 1 for a verify sequence, else 0
+  int tiles[kFusedMaxBlocks];    // per sequence: key tiles of each of its blocks
+  int fv_seq[kFusedMaxBlocks];   // per verify sequence j: its index,
+  int fv_off[kFusedMaxBlocks];   // the first unit of its blocks,
+  int fv_tiles[kFusedMaxBlocks]; // its tiles per block
+};
+static_assert(sizeof(FusedScratch) <= kKStages * kKVTile, "fused-plan scratch fits the K stages");
+
+// Step 1, every thread: thread s < num_seqs reads its sequence and stages its units.
+__device__ __forceinline__ void fused_plan_load(const Problem& p, const Pointers& ptr, FusedScratch& fs) {
+  const int s = threadIdx.x;
+  if (s < p.num_seqs) {
+    const int q0 = ptr.qsl[s], q1 = ptr.qsl[s + 1], L = ptr.seq_lens[s];
+    const int qn = q1 - q0;
+    long long v = 0;
+    int tiles = 0;
+    // the plan kernel's validity test; invalid sequences are flagged and zeroed there
+    const bool ok = qn >= 0 && q0 >= 0 && q1 <= p.T && qn <= L && (long long)L <= (long long)p.W * p.P;
+    if (ok && qn > 0 && (long long)qn * p.G <= kVerifyRows) {
+      tiles = (L + kTileKeys - 1) / kTileKeys;
+      v = ((long long)p.Hkv * (tiles + kE) << 16) | 1;
+    }
+    fs.v[s] = v;
+    fs.tiles[s] = tiles;
+  }
+}
+
+// Step 2, one warp, after a CTA barrier: the scan over sequences (each lane a contiguous
+// run of them), this CTA's range and items. Packed item: x = block, y = sequence, z = first
+// tile | tiles << 16, w = piece index | pieces << 15 | (1 << 30 if the block's first CTA's
+// range starts in an earlier block).
+__device__ __forceinline__ void fused_plan_warp(const Problem& p, Misc& ms, FusedScratch& fs, int num_ctas,
+                                                int lane) {
+  const int n = p.num_seqs;
+  const int per = (n + 31) / 32;
+  const int s0 = lane * per, s1 = min(n, s0 + per);
+  long long sum = 0;
+  for (int s = s0; s < s1; ++s) sum += fs.v[s];
+  long long x = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  const long long total = __shfl_sync(0xffffffffu, x, 31);
+  const int U = (int)(total >> 16);
+  const int C = cut_ctas(U, num_ctas);
+  const int c = blockIdx.x;
+  if (c >= C) {  // warp-uniform: no range (C = 0: no verify block at all)
+    if (lane == 0) ms.fcount = 0;
+    return;
+  }
+  const Cut k = make_cut(U, C);
+  const int u0 = cut_begin(k, c), u1 = cut_begin(k, c + 1);
+  // the blocks holding u0 and u1 - 1: found by the lane whose run of sequences holds them
+  int ib = -1, il = -1;
+  long long pre = x - sum;
+  for (int s = s0; s < s1; ++s) {
+    const long long v = fs.v[s];
+    if (v) {
+      const int j = (int)(pre & 0xffff), off = (int)(pre >> 16), units = (int)(v >> 16);
+      const int tiles = fs.tiles[s], span = tiles + kE;
+      fs.fv_seq[j] = s;
+      fs.fv_off[j] = off;
+      fs.fv_tiles[j] = tiles;
+      if (u0 >= off && u0 < off + units) ib = j * p.Hkv + (u0 - off) / span;
+      if (u1 - 1 >= off && u1 - 1 < off + units) {
+        const int kvh = (u1 - 1 - off) / span;
+        // u1 - 1 in that block's fixed-cost units: none of its tiles is in this range
+        il = j * p.Hkv + kvh - (u1 - 1 < off + kvh * span + kE ? 1 : 0);
+      }
+    }
+    pre += v;
+  }
+  ib = __reduce_max_sync(0xffffffffu, ib);
+  il = __reduce_max_sync(0xffffffffu, il);
+  __syncwarp();  // the per-verify-sequence arrays are complete
+  const int cnt = max(0, il - ib + 1);
+  for (int t = lane; t < cnt; t += 32) {
+    const int b = ib + t;
+    const int j = b / p.Hkv, kvh = b - j * p.Hkv;
+    const int tiles = fs.fv_tiles[j];
+    const int off = fs.fv_off[j] + kvh * (tiles + kE), real = off + kE;
+    const int lo = max(u0, real), hi = min(u1, real + tiles);
+    const int c0 = cut_cta(k, real);
+    const int nsplit = cut_cta(k, real + tiles - 1) - c0 + 1;
+    const int later = cut_begin(k, c0) < off ? 1 : 0;
+    ms.fitem[t] = make_int4(b, fs.fv_seq[j], (lo - real) | ((hi - lo) << 16), (c - c0) | (nsplit << 15) | (later << 30));
+  }
+  if (lane == 0) ms.fcount = cnt;
+}
+
+// Item it of a self-planned CTA (fused_plan's packing).
+__device__ __forceinline__ Item load_item_fused(const Problem& p, const Pointers& ptr, const Misc& ms, int it) {
+  const int4 f = ms.fitem[it];
+  Item r;
+  r.block = f.x;
+  r.seq = f.y;
+  r.kvh = f.x % p.Hkv;
+  r.tile_begin = f.z & 0xffff;
+  r.ntiles = (int)((unsigned)f.z >> 16);
+  r.split = f.w & 0x7fff;
+  r.nsplit = (f.w >> 15) & 0x7fff;
+  r.slot_base = split_slot_base((int)blockIdx.x - r.split, (f.w >> 30) & 1);
+  r.q0 = ptr.qsl[r.seq];
+  r.qn = ptr.qsl[r.seq + 1] - r.q0;
+  r.L = ptr.seq_lens[r.seq];
+  r.row0 = 0;
+  r.nrows = r.qn * p.G;
+  r.kv_end = r.L;  // the causal limit of the last row (token qn - 1) is L
+  r.kv_hi = min((r.tile_begin + r.ntiles) * kTileKeys, r.kv_end);
+  return r;
+}
+
+template <bool kFused>
+__device__ __forceinline__ Item load_item(const Problem& p, const ClassPlan& cp, const Pointers& ptr,
+                                          const Misc& ms, int it) {
+  if (kFused) return load_item_fused(p, ptr, ms, it);
   const WorkItem w = cp.items[it];
   const RowBlock b = cp.blocks[w.block];
   Item r;
@@ -162,7 +314,7 @@ __device__ __forceinline__ float2 bf2(uint32_t w) {
 
 }  // namespace
 
-template <int kQM>
+template <int kQM, bool kFused>
 __global__ void __launch_bounds__(kVThreads, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  Problem p, Pointers ptr, ClassPlan cp) {
@@ -177,12 +329,20 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   volatile int* abort_flag = &ms.abort_flag;
 
   auto bar = [&](const uint64_t& b) { return smem_u32(&b); };
-  // The plan is read once the previous grid (the plan kernel) has completed. A CTA with no
-  // work (an empty class, or fewer items than CTAs) leaves before any set-up.
+  // The plan is read once the previous grid (the plan kernel) has completed; a self-planned
+  // CTA works out its own items first. A CTA with no work (an empty class, or fewer items
+  // than CTAs) leaves before any set-up.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int item_begin = cp.cta_item_begin[blockIdx.x];
-  const int item_end = cp.cta_item_begin[blockIdx.x + 1];
-  if (item_begin >= item_end) return;
+  int item_begin = 0, item_end = 0;
+  FusedScratch& fs = *reinterpret_cast<FusedScratch*>(smem + kOffK);
+  if (kFused) {
+    // The sequences' reads go out first; the set-up below overlaps them.
+    fused_plan_load(p, ptr, fs);
+  } else {
+    item_begin = cp.cta_item_begin[blockIdx.x];
+    item_end = cp.cta_item_begin[blockIdx.x + 1];
+    if (item_begin >= item_end) return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKStages; ++s) {
@@ -216,10 +376,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     tmem_alloc(smem_u32(&ms.tmem_base), kTmemCols);
     tmem_relinquish();
   }
+  if (kFused) {
+    __syncthreads();  // the sequences are staged
+    if (warp == 1) fused_plan_warp(p, ms, fs, cp.num_ctas, lane);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
+  if (kFused) {
+    item_end = ms.fcount;
+    if (item_end == 0) {  // no range or no tile in it: give the columns back and leave
+      if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+      return;
+    }
+  }
   // The next kernel on the stream (the other class) may start its own checks now.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -383,9 +554,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 
     int ii = 0;
     uint32_t g = 0;
-    if (item_end > item_begin) q_prep(load_item(cp, ptr, item_begin), 0);
+    if (item_end > item_begin) q_prep(load_item<kFused>(p, cp, ptr, ms, item_begin), 0);
     for (int it = item_begin; it < item_end; ++it, ++ii) {
-      const Item I = load_item(cp, ptr, it);
+      const Item I = load_item<kFused>(p, cp, ptr, ms, it);
       const int pi = ii & 1;
       named_barrier(1, kSoftThreads);  // q_prep's shared writes (lim, m, qscale) are visible
       const float c = p.score_scale_log2 * ms.qscale[pi];
@@ -534,7 +705,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         mbar_arrive(bar(ms.p_full[g & 1]));
       }
       // Q of the next item while this item's last P.V runs
-      if (it + 1 < item_end) q_prep(load_item(cp, ptr, it + 1), ii + 1);
+      if (it + 1 < item_end) q_prep(load_item<kFused>(p, cp, ptr, ms, it + 1), ii + 1);
 
       // ---------------------------------------------------------- epilogue
       if (!mbar_wait(bar(ms.o_ready), ii & 1, abort_flag, ptr.err)) bad = true;
@@ -606,7 +777,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           if (it + 1 == item_end && I.nsplit <= kMergeMaxSplits) {
             // the CTA's last item: is this piece the block's last? (merged below)
             __threadfence();
-            ms.merge_flag = atomicAdd(&cp.counters[I.block], 1) == I.nsplit - 1;
+            ms.merge_flag = split_arrive(cp.counters + I.block, I.nsplit, split_tag(p, cp));
             __threadfence();
           }
         }
@@ -744,18 +915,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       uint32_t issued[kVStages > kKStages ? kVStages : kKStages] = {};
       bool stop = false;
       for (int it = item_begin; it < item_end && !stop; ++it) {
-        const Item I = load_item(cp, ptr, it);
-        if (is_k && pi == 0) {
-          // The softmax warps read this item's Q a few tiles from now (this warp runs ahead
-          // by its stages): bring the rows into L2 so that read does not wait on HBM.
-          for (int r = lane; r < I.nrows; r += 32) {
-            const RowMap m = map_row(I.row0 + r, p.G, I.kvh);
-            const uint8_t* row = static_cast<const uint8_t*>(ptr.q) +
-                                 ((size_t)(I.q0 + m.t) * p.q_st + (size_t)m.h * p.q_sh) * kQEsz;
-#pragma unroll
-            for (int c = 0; c < 256 * kQEsz; c += 128) prefetch_l2(row + c);
-          }
-        }
+        const Item I = load_item<kFused>(p, cp, ptr, ms, it);
         const int32_t* bt_row = ptr.block_table + (size_t)I.seq * p.bt_stride;
         const int page0 = I.tile_begin * ppt;                 // first page of the piece
         const int npages = (I.kv_hi + p.P - 1) / p.P - page0; // pages the piece reads
@@ -773,6 +933,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           return blk;
         };
         int cur = fetch(0), nxt = fetch(1);
+        if (is_k && pi == 0) {
+          // The softmax warps read this item's Q a few tiles from now (this warp runs ahead
+          // by its stages): bring the rows into L2 so that read does not wait on HBM. Issued
+          // after the block-table reads, which the first copies wait on.
+          for (int r = lane; r < I.nrows; r += 32) {
+            const RowMap m = map_row(I.row0 + r, p.G, I.kvh);
+            const uint8_t* row = static_cast<const uint8_t*>(ptr.q) +
+                                 ((size_t)(I.q0 + m.t) * p.q_st + (size_t)m.h * p.q_sh) * kQEsz;
+#pragma unroll
+            for (int c = 0; c < 256 * kQEsz; c += 128) prefetch_l2(row + c);
+          }
+        }
         int cur_w = 0;
         for (int j = 0; j < I.ntiles; ++j, ++g) {
           const int first = j * ppt;  // page of this tile, relative to the piece
@@ -824,7 +996,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         int ii = 0;
         bool ok = true;
         for (int it = item_begin; it < item_end && ok; ++it, ++ii) {
-          const Item I = load_item(cp, ptr, it);
+          const Item I = load_item<kFused>(p, cp, ptr, ms, it);
           for (int j = 0; j < I.ntiles && ok; ++j, ++g) {
             if (is_s) {
               if (j == 0 && !(ok = mbar_wait(bar(ms.q_full), ii & 1, abort_flag, ptr.err))) break;
@@ -884,7 +1056,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 }
 
 int launch_verify_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp, const pg_tensor* k,
-                     const pg_tensor* v, int sms, cudaStream_t stream) {
+                     const pg_tensor* v, int sms, cudaStream_t stream, bool dependent) {
   (void)sms;
   if (!p.kv_is_fp8) return 0;
   CUtensorMap tk, tv;
@@ -894,8 +1066,12 @@ int launch_verify_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp,
   cudaGetDevice(&dev);
   cudaError_t e;
   const int mode = p.q_cast ? kQCast : p.q_is_fp8 ? kQGiven : kQSplit;
-  auto kern = mode == kQCast ? verify_tc_kernel<kQCast> : mode == kQGiven ? verify_tc_kernel<kQGiven> : verify_tc_kernel<kQSplit>;
-  const int which = 1 << mode;
+  auto kern = p.fused_verify
+                  ? (mode == kQCast ? verify_tc_kernel<kQCast, true>
+                                    : mode == kQGiven ? verify_tc_kernel<kQGiven, true> : verify_tc_kernel<kQSplit, true>)
+                  : (mode == kQCast ? verify_tc_kernel<kQCast, false>
+                                    : mode == kQGiven ? verify_tc_kernel<kQGiven, false> : verify_tc_kernel<kQSplit, false>);
+  const int which = 1 << (mode + (p.fused_verify ? 3 : 0));
   if (dev >= 0 && dev < 64 && !(attr_done[dev] & which)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) {
@@ -917,7 +1093,7 @@ int launch_verify_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp,
     }
     attr_done[dev] |= which;
   }
-  e = launch_pdl(false, kern, cp.num_ctas, kVThreads, kSmemBytes, stream, tk, tv, p, ptr, cp);
+  e = launch_pdl(dependent, kern, cp.num_ctas, kVThreads, kSmemBytes, stream, tk, tv, p, ptr, cp);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     char buf[160];

@@ -12,7 +12,10 @@ from tests import gpu_util as gu
 
 pytestmark = pytest.mark.gpu
 
-PATHS = {"auto": 0, "warp_mma": 1}
+# auto: the tcgen05 kernels, the verify kernel planning its own class where it can;
+# warp_mma: the warp-level MMA kernel everywhere; plan_kernel: as auto, but the plan kernel
+# plans the verify class before its kernel runs.
+PATHS = {"auto": 0, "warp_mma": 1, "plan_kernel": 3}
 
 
 @pytest.fixture(params=list(PATHS))
@@ -51,20 +54,28 @@ SMALL_CASES = [
 ]
 
 
-def _assert_tcgen05_only(path):
-    """Under the automatic path every class ran on a tcgen05 kernel (path bits 2 / 4), never on
-    the warp-MMA kernel (8 / 16)."""
+def _assert_tcgen05_only(path, case=None):
+    """Under the automatic paths every class ran on a tcgen05 kernel (path bits 2 / 4), never on
+    the warp-MMA kernel (8 / 16). With an e4m3 cache and at most 512 verify blocks the
+    automatic path's verify kernel planned its own class; under plan_kernel it never does."""
     import paged_gqa_gb300 as pg
-    if path == "auto":
-        bits = pg.paged_gqa_last_plan()["path_bits"]
+    plan = pg.paged_gqa_last_plan()
+    if path in ("auto", "plan_kernel"):
+        bits = plan["path_bits"]
         assert bits & 6 and not bits & 24, f"path bits {bits}"
+    if path == "plan_kernel" or path == "warp_mma":
+        assert plan["verify_self_planned"] == 0
+    elif case is not None:
+        fp8 = case.k_cache.dtype != torch.bfloat16
+        small = case.spec.num_seqs * case.spec.num_kv_heads <= 512
+        assert plan["verify_self_planned"] == int(fp8 and small), plan
 
 
 @pytest.mark.parametrize("i", range(len(SMALL_CASES)))
 def test_small_cases_match_oracle(i, path):
     case = _small(1000 + i, **SMALL_CASES[i])
     got = gu.run_library(case)
-    _assert_tcgen05_only(path)
+    _assert_tcgen05_only(path, case)
     gu.check_full(case, got, f"case {i} path {path}")
 
 
@@ -133,6 +144,25 @@ def test_plan_beyond_shared_memory_caches(path):
     spec = wl.CaseSpec("beyond caches", seqs, 16, 8, 16)
     case = wl.make_case(spec, device="cuda", seed=21, poison=True)
     gu.check_full(case, gu.run_library(case), "beyond plan caches")
+    _assert_tcgen05_only(path, case)  # 20800 verify blocks: planned by the plan kernel
+
+
+def test_self_planned_verify_at_its_limit(path):
+    """512 verify blocks (256 sequences x 2 kv heads), the most a self-planning verify kernel
+    takes, with short and long contexts, a few empty and a few prefill sequences between
+    them, and 513 blocks (one more sequence), which the plan kernel plans."""
+    gen = torch.Generator().manual_seed(23)
+    for n in (256, 257):
+        seqs = [(int(q), int(L)) for q, L in zip(torch.randint(1, 5, (n,), generator=gen),
+                                                    torch.randint(1, 2000, (n,), generator=gen))]
+        seqs[3] = (0, 70)
+        seqs[100] = (20, 900)  # 20 tokens x G = 8: 160 rows, prefill blocks
+        seqs[200] = (0, 0)
+        seqs[-1] = (4, 9000)
+        spec = wl.CaseSpec("limit", seqs, 16, 2, 16)
+        case = wl.make_case(spec, device="cuda", seed=23 + n, poison=True)
+        gu.check_full(case, gu.run_library(case), f"{n} sequences x 2 kv heads")
+        _assert_tcgen05_only(path, case)
 
 
 def test_decode_batch(path):
@@ -242,6 +272,43 @@ def test_caller_workspace_matches_library_workspace():
         pg.paged_gqa_attn_ex(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
                              case.query_start_loc, 1.0, case.k_descale, case.v_descale, case.softmax_scale,
                              out, ws[: nbytes // 2])
+
+
+@pytest.mark.parametrize("fill", ["zeros", "ones", "random", "left_by_another_shape"])
+def test_caller_workspace_needs_no_initialisation(fill):
+    """The split counters carry a per-call tag: a caller workspace filled with any bytes,
+    or left by a call of another shape, gives the library workspace's result exactly, on
+    both planning paths and over repeated calls."""
+    import paged_gqa_gb300 as pg
+    case = _small(78, group=16, num_kv_heads=1, page_size=16, q_lens=[4, 4, 2, 3], max_ctx=20000)
+    other = _small(79, group=8, num_kv_heads=2, page_size=64, q_lens=[70, 4, 4, 1, 2], max_ctx=9000)
+    ref = gu.run_library(case)
+    nbytes = max(pg.paged_gqa_workspace_size(c.spec.num_seqs, c.spec.total_q, c.spec.num_q_heads,
+                                             c.spec.num_kv_heads, c.spec.page_size, c.block_table.shape[1], 0)
+                 for c in (case, other))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    if fill == "zeros":
+        ws.zero_()
+    elif fill == "ones":
+        ws.fill_(255)
+    elif fill == "random":
+        ws.copy_(torch.randint(0, 256, (nbytes,), generator=torch.Generator().manual_seed(5), dtype=torch.uint8))
+    else:
+        o = torch.empty(other.q.shape, dtype=torch.bfloat16, device="cuda")
+        pg.paged_gqa_attn_ex(other.q, other.k_cache, other.v_cache, other.block_table, other.seq_lens,
+                             other.query_start_loc, 1.0, other.k_descale, other.v_descale, other.softmax_scale,
+                             o, ws)
+    for path in (0, 3, 0):
+        prev = pg.paged_gqa_set_path(path)
+        try:
+            out = torch.full_like(ref, float("nan"))
+            pg.paged_gqa_attn_ex(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                                 case.query_start_loc, 1.0, case.k_descale, case.v_descale, case.softmax_scale,
+                                 out, ws)
+            assert pg.paged_gqa_check_device_errors() == 0
+        finally:
+            pg.paged_gqa_set_path(prev)
+        assert torch.equal(out, ref), f"fill {fill}, path {path}"
 
 
 def test_deterministic_across_calls():
