@@ -341,7 +341,10 @@ int run(const Validated& val, const pg_tensor* k, const pg_tensor* v, void* ws, 
   // first, and the plan kernel (prefill only) and the prefill kernel follow it as
   // programmatic dependents, off the critical path.
   const long long max_tiles = ((long long)p.W * p.P + kTileKeys - 1) / kTileKeys;
-  p.fused_verify = fast_ok && path != 3 && (long long)p.num_seqs * p.Hkv <= kFusedMaxBlocks &&
+  // A single sequence whose q_len x G rows exceed a verify block is all prefill (its q_len is
+  // T): then the plan kernel goes first, as the verify kernel would only find nothing to do.
+  const bool single_prefill = p.num_seqs == 1 && (long long)p.T * p.G > kVerifyRows;
+  p.fused_verify = fast_ok && path != 3 && !single_prefill && (long long)p.num_seqs * p.Hkv <= kFusedMaxBlocks &&
                    max_tiles < (1 << 16) &&
                    (long long)p.num_seqs * p.Hkv * (max_tiles + fixed_cost(0)) < (1LL << 31);
   if (!p.fused_verify) {

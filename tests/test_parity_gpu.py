@@ -68,7 +68,8 @@ def _assert_tcgen05_only(path, case=None):
     elif case is not None:
         fp8 = case.k_cache.dtype != torch.bfloat16
         small = case.spec.num_seqs * case.spec.num_kv_heads <= 512
-        assert plan["verify_self_planned"] == int(fp8 and small), plan
+        single_prefill = case.spec.num_seqs == 1 and case.spec.total_q * case.spec.group > 64
+        assert plan["verify_self_planned"] == int(fp8 and small and not single_prefill), plan
 
 
 @pytest.mark.parametrize("i", range(len(SMALL_CASES)))
