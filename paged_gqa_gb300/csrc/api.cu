@@ -336,7 +336,7 @@ int run(const Validated& val, const pg_tensor* k, const pg_tensor* v, void* ws, 
     ++launched;
   }
   p.call_tag = next_call_tag();
-  // The verify kernel plans its own class when its CTAs can hold one entry per verify block
+  // The verify kernel (FP8 or bf16) plans its own class when its CTAs can hold one entry per verify block
   // (sequence x kv head), the class's units fit 31 bits and a block's tiles 16: it then runs
   // first, and the plan kernel (prefill only) and the prefill kernel follow it as
   // programmatic dependents, off the critical path.
@@ -344,7 +344,7 @@ int run(const Validated& val, const pg_tensor* k, const pg_tensor* v, void* ws, 
   // A single sequence whose q_len x G rows exceed a verify block is all prefill (its q_len is
   // T): then the plan kernel goes first, as the verify kernel would only find nothing to do.
   const bool single_prefill = p.num_seqs == 1 && (long long)p.T * p.G > kVerifyRows;
-  p.fused_verify = fast_ok && path != 3 && !single_prefill && (long long)p.num_seqs * p.Hkv <= kFusedMaxBlocks &&
+  p.fused_verify = (fast_ok || bf16_ok) && path != 3 && !single_prefill && (long long)p.num_seqs * p.Hkv <= kFusedMaxBlocks &&
                    max_tiles < (1 << 16) &&
                    (long long)p.num_seqs * p.Hkv * (max_tiles + fixed_cost(0)) < (1LL << 31);
   if (!p.fused_verify) {
@@ -370,7 +370,7 @@ int run(const Validated& val, const pg_tensor* k, const pg_tensor* v, void* ws, 
       // verify kernel planned itself) as a programmatic dependent, when that one is a
       // tcgen05 kernel too and no event sits between them
       const bool dependent = c == 1 && !ev0 && (after_plan || ((used & 2) && !prev_ev));
-      int r = bf16_ok ? launch_bf16_tc(p, ptr, cp[c], k, v, stream, dependent)
+      int r = bf16_ok ? launch_bf16_tc(p, ptr, cp[c], k, v, stream, dependent, c == 0 && p.fused_verify)
               : (c == 0) ? launch_verify_tc(p, ptr, cp[c], k, v, ds->sms, stream, !p.fused_verify && pdl_enabled())
                          : launch_prefill_tc(p, ptr, cp[c], k, v, ds->sms, stream, dependent);
       if (r < 0) return fail(PG_ERR_CUDA, "tcgen05 %s launch failed: %s", c == 0 ? "verify" : "prefill",

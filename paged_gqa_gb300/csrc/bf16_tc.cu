@@ -28,6 +28,7 @@
 
 #include "common.cuh"
 #include "device_util.cuh"
+#include "self_plan.cuh"
 #include "tc_kernels.cuh"
 #include "tc_util.cuh"
 
@@ -80,10 +81,15 @@ struct Misc {
   uint32_t tmem_base;
   int abort_flag;
   int merge_flag;
+  // Self-planned verify class (Problem::fused_verify, class-0 launch): this CTA's items,
+  // packed by self_plan::plan_warp, and their count.
+  int4 fitem[kFusedMaxBlocks];
+  int fcount;
 };
 static_assert(offsetof(Misc, red) % 16 == 0 && offsetof(Misc, k_full) % 8 == 0, "Misc alignment");
 constexpr size_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
 static_assert(kSmemBytes <= 232448, "fits the dynamic shared memory of a CTA");
+static_assert(sizeof(self_plan::Scratch) <= kKStages * kKVTile, "the self-plan scratch fits the K stages");
 
 struct Item {
   int block, seq, kvh, row0, nrows, kv_end, nsplit, split, slot_base;
@@ -93,7 +99,29 @@ struct Item {
 
 // A work item of the plan (128-key tiles) as 64-key sub-tiles that end at the piece's last
 // key: sub-tiles past it would read block-table entries the call does not define.
-__device__ __forceinline__ Item load_item(const ClassPlan& cp, const Pointers& ptr, int it) {
+template <bool kFused>
+__device__ __forceinline__ Item load_item(const Problem& p, const ClassPlan& cp, const Pointers& ptr,
+                                          const Misc& ms, int it) {
+  if (kFused) {  // a verify block of a self-planned CTA
+    const self_plan::Piece f = self_plan::unpack(p, ms.fitem[it]);
+    Item r;
+    r.block = f.block;
+    r.seq = f.seq;
+    r.kvh = f.kvh;
+    r.nsplit = f.nsplit;
+    r.split = f.split;
+    r.slot_base = f.slot_base;
+    r.tile_begin = f.tile_begin;
+    r.q0 = ptr.qsl[r.seq];
+    r.qn = ptr.qsl[r.seq + 1] - r.q0;
+    r.L = ptr.seq_lens[r.seq];
+    r.row0 = 0;
+    r.nrows = r.qn * p.G;
+    r.kv_end = r.L;  // the causal limit of the last row (token qn - 1) is L
+    r.kv_hi = min((f.tile_begin + f.ntiles) * kTileKeys, r.kv_end);
+    r.nsub = (r.kv_hi - f.tile_begin * kTileKeys + kSub - 1) / kSub;
+    return r;
+  }
   const WorkItem w = cp.items[it];
   const RowBlock b = cp.blocks[w.block];
   Item r;
@@ -117,6 +145,7 @@ __device__ __forceinline__ Item load_item(const ClassPlan& cp, const Pointers& p
 
 }  // namespace
 
+template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                Problem p, Pointers ptr, ClassPlan cp) {
@@ -127,11 +156,18 @@ bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &ms.abort_flag;
   auto bar = [&](const uint64_t& b) { return smem_u32(&b); };
-  // The plan is read once the previous grid has completed. A CTA with no work leaves at once.
+  // The plan is read once the previous grid has completed; a self-planned CTA works out its
+  // own items first (self_plan.cuh). A CTA with no work leaves before any set-up.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int item_begin = cp.cta_item_begin[blockIdx.x];
-  const int item_end = cp.cta_item_begin[blockIdx.x + 1];
-  if (item_begin >= item_end) return;
+  int item_begin = 0, item_end = 0;
+  self_plan::Scratch& fs = *reinterpret_cast<self_plan::Scratch*>(smem + kOffK);
+  if (kFused) {
+    self_plan::load(p, ptr, fs);  // the set-up below overlaps these reads
+  } else {
+    item_begin = cp.cta_item_begin[blockIdx.x];
+    item_end = cp.cta_item_begin[blockIdx.x + 1];
+    if (item_begin >= item_end) return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKStages; ++s) {
@@ -161,10 +197,21 @@ bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
     tmem_alloc(smem_u32(&ms.tmem_base), kTmemCols);
     tmem_relinquish();
   }
+  if (kFused) {
+    __syncthreads();  // the sequences are staged
+    if (warp == 0) self_plan::plan_warp(p, fs, cp.num_ctas, lane, ms.fitem, &ms.fcount);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
+  if (kFused) {
+    item_end = ms.fcount;
+    if (item_end == 0) {  // no range or no tile in it: give the columns back and leave
+      if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+      return;
+    }
+  }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0 || warp == kVProducerWarp) {
@@ -183,25 +230,27 @@ bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
     uint32_t issued[kVStages > kKStages ? kVStages : kKStages] = {};
     bool stop = false;
     for (int it = item_begin; it < item_end && !stop; ++it) {
-      const Item I = load_item(cp, ptr, it);
+      const Item I = load_item<kFused>(p, cp, ptr, ms, it);
       const int32_t* bt_row = ptr.block_table + (size_t)I.seq * p.bt_stride;
       const int key_begin = I.tile_begin * kTileKeys;     // a multiple of P (P divides 128)
       const int page0 = key_begin / p.P;                  // first page of the piece
       const int npages = (I.kv_hi + p.P - 1) / p.P - page0;
       // a window of 32 block-table entries, one per lane, and the next one in flight
-      auto fetch = [&](int w) -> int {
-        const int pg = w * 32 + lane;
-        int blk = -1;
-        if (pg < npages) {
-          blk = bt_row[page0 + pg];
-          if (blk < 0 || blk >= p.NB) {
-            atomicOr(ptr.err, kErrPage);
-            blk = 0;
-          }
+      // The window's entries are loaded without waiting for the piece's page count (its
+      // sequence length may still be on its way): the index is clamped to the row, and an
+      // entry is checked, or dropped past the piece's pages, when it is used.
+      auto fetch_raw = [&](int w) -> int { return bt_row[min(page0 + w * 32 + lane, p.W - 1)]; };
+      auto check = [&](int w, int raw) -> int {
+        if (w * 32 + lane >= npages) return -1;
+        if (raw < 0 || raw >= p.NB) {
+          atomicOr(ptr.err, kErrPage);
+          return 0;
         }
-        return blk;
+        return raw;
       };
-      int cur = fetch(0), nxt = fetch(1);
+      auto fetch = [&](int w) -> int { return check(w, fetch_raw(w)); };
+      const int raw0 = fetch_raw(0), raw1 = fetch_raw(1);
+      int cur = check(0, raw0), nxt = check(1, raw1);
       int cur_w = 0;
       for (int s = 0; s < I.nsub; ++s, ++g) {
         const int first = (s * kSub) / p.P;      // page of this sub-tile, relative to the piece
@@ -251,7 +300,7 @@ bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
       int ii = 0;
       bool ok = true;
       for (int it = item_begin; it < item_end && ok; ++it, ++ii) {
-        const Item I = load_item(cp, ptr, it);
+        const Item I = load_item<kFused>(p, cp, ptr, ms, it);
         for (int j = 0; j < I.nsub && ok; ++j, ++g) {
           const uint32_t b = g & 1;
           if (is_s) {
@@ -360,9 +409,9 @@ bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
     int ii = 0;
     uint32_t g = 0;
     const float c = p.score_scale_log2;
-    if (item_end > item_begin) q_prep(load_item(cp, ptr, item_begin), 0);
+    if (item_end > item_begin) q_prep(load_item<kFused>(p, cp, ptr, ms, item_begin), 0);
     for (int it = item_begin; it < item_end; ++it, ++ii) {
-      const Item I = load_item(cp, ptr, it);
+      const Item I = load_item<kFused>(p, cp, ptr, ms, it);
       const int pi = ii & 1;
       named_barrier(9, kSoftThreads);  // q_prep's shared writes are visible
       const int lim = ms.lim[pi][row];
@@ -468,7 +517,7 @@ bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
             !mbar_wait(bar(ms.pv_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, abort_flag, ptr.err))
           bad = true;
       }
-      if (it + 1 < item_end) q_prep(load_item(cp, ptr, it + 1), ii + 1);
+      if (it + 1 < item_end) q_prep(load_item<kFused>(p, cp, ptr, ms, it + 1), ii + 1);
 
       // ---------------------------------------------------------- epilogue
       if (!mbar_wait(bar(ms.o_ready), ii & 1, abort_flag, ptr.err)) bad = true;
@@ -535,7 +584,7 @@ bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
 }
 
 int launch_bf16_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp, const pg_tensor* k,
-                   const pg_tensor* v, cudaStream_t stream, bool dependent) {
+                   const pg_tensor* v, cudaStream_t stream, bool dependent, bool self_planned) {
   if (p.kv_is_fp8 || p.q_is_fp8 || p.q_cast) return 0;
   CUtensorMap tk, tv;
   if (!make_cache_tmap(&tk, k, p.P) || !make_cache_tmap(&tv, v, p.P)) return -1;
@@ -543,17 +592,19 @@ int launch_bf16_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp, c
   int dev = 0;
   cudaGetDevice(&dev);
   cudaError_t e;
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    e = cudaFuncSetAttribute(bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  auto kern = self_planned ? bf16_tc_kernel<true> : bf16_tc_kernel<false>;
+  const int which = self_planned ? 2 : 1;
+  if (dev >= 0 && dev < 64 && !(attr_done[dev] & which)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) {
       char buf[160];
       snprintf(buf, sizeof buf, "cudaFuncSetAttribute(bf16): %s", cudaGetErrorString(e));
       set_tc_error(buf);
       return -1;
     }
-    attr_done[dev] = 1;
+    attr_done[dev] |= which;
   }
-  e = launch_pdl(dependent, bf16_tc_kernel, cp.num_ctas, kThreads, kSmemBytes, stream, tk, tv, p, ptr, cp);
+  e = launch_pdl(dependent, kern, cp.num_ctas, kThreads, kSmemBytes, stream, tk, tv, p, ptr, cp);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     char buf[160];

@@ -20,9 +20,10 @@ int launch_verify_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp,
 // verify-class kernel), so its CTAs are already resident when that kernel ends.
 int launch_prefill_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp, const pg_tensor* k,
                       const pg_tensor* v, int sms, cudaStream_t stream, bool dependent);
-// bf16 q and bf16 caches, either class of row blocks (bf16_tc.cu).
+// bf16 q and bf16 caches, either class of row blocks (bf16_tc.cu). self_planned: the
+// verify-class launch of a call with Problem::fused_verify (its CTAs plan the class).
 int launch_bf16_tc(const Problem& p, const Pointers& ptr, const ClassPlan& cp, const pg_tensor* k,
-                   const pg_tensor* v, cudaStream_t stream, bool dependent);
+                   const pg_tensor* v, cudaStream_t stream, bool dependent, bool self_planned);
 const char* tc_last_error();
 void set_tc_error(const char* msg);
 // TMA map over an e4m3 or bf16 cache [NB, P, Hkv, 256] (128 bytes of d of one page per box).

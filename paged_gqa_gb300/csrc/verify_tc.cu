@@ -44,6 +44,7 @@
 
 #include "common.cuh"
 #include "device_util.cuh"
+#include "self_plan.cuh"
 #include "tc_kernels.cuh"
 #include "tc_util.cuh"
 
@@ -124,14 +125,14 @@ struct Misc {
   int abort_flag;
   int merge_flag;
   // Self-planned verify class (Problem::fused_verify): this CTA's items, packed by
-  // fused_plan, their count, and the CTA-wide scan's warp totals.
+  // self_plan::plan_warp, and their count.
   int4 fitem[kFusedMaxBlocks];
-  long long scan_warp[kVThreads / 32];
   int fcount;
 };
 static_assert(offsetof(Misc, m) % 16 == 0 && offsetof(Misc, k_full) % 8 == 0, "Misc alignment");
 constexpr size_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
+static_assert(sizeof(self_plan::Scratch) <= kKStages * kKVTile, "the self-plan scratch fits the K stages");
 
 struct Item {
   int block, seq, kvh, row0, nrows, kv_end, nsplit, split, slot_base;
@@ -139,139 +140,18 @@ struct Item {
   int q0, qn, L;
 };
 
-constexpr int kE = fixed_cost(0);
-
-// Self-planned verify class: every CTA works out the plan kernel's cut of the verify blocks
-// (one per verify sequence and kv head, in sequence order, each fixed_cost(0) units and
-// then its ceil(L / 128) key tiles) from query_start_loc and seq_lens, and keeps its own
-// items in shared memory; nothing is written to global memory. The host guarantees
-// num_seqs * Hkv <= kFusedMaxBlocks (so num_seqs < the CTA's threads), U < 2^31 and key
-// tiles per block < 2^16.
-//
-// The cut in 32-bit arithmetic: with U = q C + r, range c starts at floor(c U / C) =
-// c q + floor(c r / C) (c r < 2^20), and the range holding unit u comes from a float
-// estimate of u C / U (off by at most one) and a correction.
-struct Cut {
-  int U, C, q, r;
-};
-__device__ __forceinline__ Cut make_cut(int U, int C) { return Cut{U, C, U / C, U % C}; }
-__device__ __forceinline__ int cut_begin(const Cut& k, int c) {
-  return c * k.q + (int)(((unsigned)c * (unsigned)k.r) / (unsigned)k.C);
-}
-__device__ __forceinline__ int cut_cta(const Cut& k, int u) {
-  int c = (int)((float)u * (float)k.C / (float)k.U);
-  c = min(max(c, 0), k.C - 1);
-  while (c > 0 && cut_begin(k, c) > u) --c;
-  while (c + 1 < k.C && cut_begin(k, c + 1) <= u) ++c;
-  return c;
-}
-
-// Scratch of the self-planned prologue, in the K stages (no copy has touched them yet).
-struct FusedScratch {
-  long long v[kFusedMaxBlocks];  // per sequence: (units << 16) | 1 for a verify sequence, else 0
-  int tiles[kFusedMaxBlocks];    // per sequence: key tiles of each of its blocks
-  int fv_seq[kFusedMaxBlocks];   // per verify sequence j: its index,
-  int fv_off[kFusedMaxBlocks];   // the first unit of its blocks,
-  int fv_tiles[kFusedMaxBlocks]; // its tiles per block
-};
-static_assert(sizeof(FusedScratch) <= kKStages * kKVTile, "fused-plan scratch fits the K stages");
-
-// Step 1, every thread: thread s < num_seqs reads its sequence and stages its units.
-__device__ __forceinline__ void fused_plan_load(const Problem& p, const Pointers& ptr, FusedScratch& fs) {
-  const int s = threadIdx.x;
-  if (s < p.num_seqs) {
-    const int q0 = ptr.qsl[s], q1 = ptr.qsl[s + 1], L = ptr.seq_lens[s];
-    const int qn = q1 - q0;
-    long long v = 0;
-    int tiles = 0;
-    // the plan kernel's validity test; invalid sequences are flagged and zeroed there
-    const bool ok = qn >= 0 && q0 >= 0 && q1 <= p.T && qn <= L && (long long)L <= (long long)p.W * p.P;
-    if (ok && qn > 0 && (long long)qn * p.G <= kVerifyRows) {
-      tiles = (L + kTileKeys - 1) / kTileKeys;
-      v = ((long long)p.Hkv * (tiles + kE) << 16) | 1;
-    }
-    fs.v[s] = v;
-    fs.tiles[s] = tiles;
-  }
-}
-
-// Step 2, one warp, after a CTA barrier: the scan over sequences (each lane a contiguous
-// run of them), this CTA's range and items. Packed item: x = block, y = sequence, z = first
-// tile | tiles << 16, w = piece index | pieces << 15 | (1 << 30 if the block's first CTA's
-// range starts in an earlier block).
-__device__ __forceinline__ void fused_plan_warp(const Problem& p, Misc& ms, FusedScratch& fs, int num_ctas,
-                                                int lane) {
-  const int n = p.num_seqs;
-  const int per = (n + 31) / 32;
-  const int s0 = lane * per, s1 = min(n, s0 + per);
-  long long sum = 0;
-  for (int s = s0; s < s1; ++s) sum += fs.v[s];
-  long long x = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  const long long total = __shfl_sync(0xffffffffu, x, 31);
-  const int U = (int)(total >> 16);
-  const int C = cut_ctas(U, num_ctas);
-  const int c = blockIdx.x;
-  if (c >= C) {  // warp-uniform: no range (C = 0: no verify block at all)
-    if (lane == 0) ms.fcount = 0;
-    return;
-  }
-  const Cut k = make_cut(U, C);
-  const int u0 = cut_begin(k, c), u1 = cut_begin(k, c + 1);
-  // the blocks holding u0 and u1 - 1: found by the lane whose run of sequences holds them
-  int ib = -1, il = -1;
-  long long pre = x - sum;
-  for (int s = s0; s < s1; ++s) {
-    const long long v = fs.v[s];
-    if (v) {
-      const int j = (int)(pre & 0xffff), off = (int)(pre >> 16), units = (int)(v >> 16);
-      const int tiles = fs.tiles[s], span = tiles + kE;
-      fs.fv_seq[j] = s;
-      fs.fv_off[j] = off;
-      fs.fv_tiles[j] = tiles;
-      if (u0 >= off && u0 < off + units) ib = j * p.Hkv + (u0 - off) / span;
-      if (u1 - 1 >= off && u1 - 1 < off + units) {
-        const int kvh = (u1 - 1 - off) / span;
-        // u1 - 1 in that block's fixed-cost units: none of its tiles is in this range
-        il = j * p.Hkv + kvh - (u1 - 1 < off + kvh * span + kE ? 1 : 0);
-      }
-    }
-    pre += v;
-  }
-  ib = __reduce_max_sync(0xffffffffu, ib);
-  il = __reduce_max_sync(0xffffffffu, il);
-  __syncwarp();  // the per-verify-sequence arrays are complete
-  const int cnt = max(0, il - ib + 1);
-  for (int t = lane; t < cnt; t += 32) {
-    const int b = ib + t;
-    const int j = b / p.Hkv, kvh = b - j * p.Hkv;
-    const int tiles = fs.fv_tiles[j];
-    const int off = fs.fv_off[j] + kvh * (tiles + kE), real = off + kE;
-    const int lo = max(u0, real), hi = min(u1, real + tiles);
-    const int c0 = cut_cta(k, real);
-    const int nsplit = cut_cta(k, real + tiles - 1) - c0 + 1;
-    const int later = cut_begin(k, c0) < off ? 1 : 0;
-    ms.fitem[t] = make_int4(b, fs.fv_seq[j], (lo - real) | ((hi - lo) << 16), (c - c0) | (nsplit << 15) | (later << 30));
-  }
-  if (lane == 0) ms.fcount = cnt;
-}
-
-// Item it of a self-planned CTA (fused_plan's packing).
+// Item it of a self-planned CTA.
 __device__ __forceinline__ Item load_item_fused(const Problem& p, const Pointers& ptr, const Misc& ms, int it) {
-  const int4 f = ms.fitem[it];
+  const self_plan::Piece f = self_plan::unpack(p, ms.fitem[it]);
   Item r;
-  r.block = f.x;
-  r.seq = f.y;
-  r.kvh = f.x % p.Hkv;
-  r.tile_begin = f.z & 0xffff;
-  r.ntiles = (int)((unsigned)f.z >> 16);
-  r.split = f.w & 0x7fff;
-  r.nsplit = (f.w >> 15) & 0x7fff;
-  r.slot_base = split_slot_base((int)blockIdx.x - r.split, (f.w >> 30) & 1);
+  r.block = f.block;
+  r.seq = f.seq;
+  r.kvh = f.kvh;
+  r.tile_begin = f.tile_begin;
+  r.ntiles = f.ntiles;
+  r.split = f.split;
+  r.nsplit = f.nsplit;
+  r.slot_base = f.slot_base;
   r.q0 = ptr.qsl[r.seq];
   r.qn = ptr.qsl[r.seq + 1] - r.q0;
   r.L = ptr.seq_lens[r.seq];
@@ -334,10 +214,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   // than CTAs) leaves before any set-up.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   int item_begin = 0, item_end = 0;
-  FusedScratch& fs = *reinterpret_cast<FusedScratch*>(smem + kOffK);
+  self_plan::Scratch& fs = *reinterpret_cast<self_plan::Scratch*>(smem + kOffK);
   if (kFused) {
     // The sequences' reads go out first; the set-up below overlaps them.
-    fused_plan_load(p, ptr, fs);
+    self_plan::load(p, ptr, fs);
   } else {
     item_begin = cp.cta_item_begin[blockIdx.x];
     item_end = cp.cta_item_begin[blockIdx.x + 1];
@@ -378,7 +258,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   }
   if (kFused) {
     __syncthreads();  // the sequences are staged
-    if (warp == 1) fused_plan_warp(p, ms, fs, cp.num_ctas, lane);
+    if (warp == 1) self_plan::plan_warp(p, fs, cp.num_ctas, lane, ms.fitem, &ms.fcount);
   }
   tc_fence_before();
   __syncthreads();
@@ -920,19 +800,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         const int page0 = I.tile_begin * ppt;                 // first page of the piece
         const int npages = (I.kv_hi + p.P - 1) / p.P - page0; // pages the piece reads
         // a window of 32 block-table entries, one per lane, and the next one in flight
-        auto fetch = [&](int w) -> int {
-          const int pg = w * 32 + lane;
-          int blk = -1;
-          if (pg < npages) {
-            blk = bt_row[page0 + pg];
-            if (blk < 0 || blk >= p.NB) {
-              atomicOr(ptr.err, kErrPage);
-              blk = 0;
-            }
+        // The window's entries are loaded without waiting for the piece's page count (its
+        // sequence length may still be on its way): the index is clamped to the row, and an
+        // entry is checked, or dropped past the piece's pages, when it is used.
+        auto fetch_raw = [&](int w) -> int { return bt_row[min(page0 + w * 32 + lane, p.W - 1)]; };
+        auto check = [&](int w, int raw) -> int {
+          if (w * 32 + lane >= npages) return -1;
+          if (raw < 0 || raw >= p.NB) {
+            atomicOr(ptr.err, kErrPage);
+            return 0;
           }
-          return blk;
+          return raw;
         };
-        int cur = fetch(0), nxt = fetch(1);
+        auto fetch = [&](int w) -> int { return check(w, fetch_raw(w)); };
+        const int raw0 = fetch_raw(0), raw1 = fetch_raw(1);
+        int cur = check(0, raw0), nxt = check(1, raw1);
         if (is_k && pi == 0) {
           // The softmax warps read this item's Q a few tiles from now (this warp runs ahead
           // by its stages): bring the rows into L2 so that read does not wait on HBM. Issued

@@ -56,8 +56,8 @@ SMALL_CASES = [
 
 def _assert_tcgen05_only(path, case=None):
     """Under the automatic paths every class ran on a tcgen05 kernel (path bits 2 / 4), never on
-    the warp-MMA kernel (8 / 16). With an e4m3 cache and at most 512 verify blocks the
-    automatic path's verify kernel planned its own class; under plan_kernel it never does."""
+    the warp-MMA kernel (8 / 16). With at most 512 verify blocks the automatic path's verify
+    kernel (FP8 or bf16) planned its own class; under plan_kernel it never does."""
     import paged_gqa_gb300 as pg
     plan = pg.paged_gqa_last_plan()
     if path in ("auto", "plan_kernel"):
@@ -66,10 +66,10 @@ def _assert_tcgen05_only(path, case=None):
     if path == "plan_kernel" or path == "warp_mma":
         assert plan["verify_self_planned"] == 0
     elif case is not None:
-        fp8 = case.k_cache.dtype != torch.bfloat16
+        tc = case.k_cache.dtype != torch.bfloat16 or case.q.dtype == torch.bfloat16  # a tcgen05 verify kernel
         small = case.spec.num_seqs * case.spec.num_kv_heads <= 512
         single_prefill = case.spec.num_seqs == 1 and case.spec.total_q * case.spec.group > 64
-        assert plan["verify_self_planned"] == int(fp8 and small and not single_prefill), plan
+        assert plan["verify_self_planned"] == int(tc and small and not single_prefill), plan
 
 
 @pytest.mark.parametrize("i", range(len(SMALL_CASES)))
@@ -97,7 +97,7 @@ BF16_CASES = [
 def test_bf16_cache_cases_match_oracle(i, path):
     case = _small(1100 + i, kv_dtype="bf16", **BF16_CASES[i])
     got = gu.run_library(case)
-    _assert_tcgen05_only(path)
+    _assert_tcgen05_only(path, case)
     gu.check_full(case, got, f"bf16 case {i} path {path}")
 
 
@@ -105,14 +105,14 @@ def test_bf16_long_sequence_is_split(path):
     spec = wl.CaseSpec("long bf16", [(4, 30000)], 16, 1, 16, kv_dtype="bf16")
     case = wl.make_case(spec, device="cuda", seed=14, poison=True)
     got = gu.run_library(case)
-    _assert_tcgen05_only(path)
+    _assert_tcgen05_only(path, case)
     gu.check_full(case, got, "long split bf16")
 
 
 def test_config1_tiny_verify(path):
     case = wl.make_case(wl.config_spec(1), device="cuda", seed=0, poison=True)
     got = gu.run_library(case)
-    _assert_tcgen05_only(path)
+    _assert_tcgen05_only(path, case)
     gu.check_full(case, got, "config 1")
 
 
