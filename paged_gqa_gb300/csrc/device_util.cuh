@@ -103,8 +103,13 @@ __device__ __forceinline__ unsigned long long split_tag(const Problem& p, const 
 // One piece of a split block has stored its partial; true for the block's last piece. The
 // counter word holds (tag << 16) | arrivals (nsplit < 2^16); a word with another tag counts
 // as no arrivals. The CAS loop retries only while other pieces of the block arrive.
-__device__ __forceinline__ bool split_arrive(unsigned long long* counter, int nsplit, unsigned long long tag) {
-  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(counter);
+// split_peek reads the word for split_arrive_from, so that its round trip can overlap the
+// wait for the piece's partial; split_arrive reads it itself.
+__device__ __forceinline__ unsigned long long split_peek(const unsigned long long* counter) {
+  return *reinterpret_cast<const volatile unsigned long long*>(counter);
+}
+__device__ __forceinline__ bool split_arrive_from(unsigned long long* counter, unsigned long long old, int nsplit,
+                                                  unsigned long long tag) {
   for (;;) {
     const unsigned arrived = (old >> 16) == tag ? (unsigned)(old & 0xffffu) : 0u;
     const unsigned long long want = (tag << 16) | (arrived + 1u);
@@ -112,6 +117,9 @@ __device__ __forceinline__ bool split_arrive(unsigned long long* counter, int ns
     if (seen == old) return arrived + 1u == (unsigned)nsplit;
     old = seen;
   }
+}
+__device__ __forceinline__ bool split_arrive(unsigned long long* counter, int nsplit, unsigned long long tag) {
+  return split_arrive_from(counter, split_peek(counter), nsplit, tag);
 }
 
 // Called by `nthreads` threads (ids tid = 0..nthreads-1) that share barrier `bar_id`,

@@ -649,15 +649,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         fence_proxy_async_smem();
         named_barrier(1, kSoftThreads);
         if (gi == 0) {
+          const bool last_item = it + 1 == item_end && I.nsplit <= kMergeMaxSplits;
+          // the counter's current word travels while the partial is written
+          const unsigned long long seen = last_item ? split_peek(cp.counters + I.block) : 0ull;
           bulk_store(slot_o(cp, slot), smem_u32(stage), (uint32_t)I.nrows * kHeadDim * 2u);
           bulk_store(slot_lse(cp, slot), smem_u32(ms.lse_stage), kVN * 4u);  // all 64 entries of the slot
           bulk_commit();
           bulk_wait_all();  // the partial is in global memory before the split counter moves
           fence_proxy_async_global();
-          if (it + 1 == item_end && I.nsplit <= kMergeMaxSplits) {
+          if (last_item) {
             // the CTA's last item: is this piece the block's last? (merged below)
             __threadfence();
-            ms.merge_flag = split_arrive(cp.counters + I.block, I.nsplit, split_tag(p, cp));
+            ms.merge_flag = split_arrive_from(cp.counters + I.block, seen, I.nsplit, split_tag(p, cp));
             __threadfence();
           }
         }
