@@ -42,7 +42,7 @@ constexpr uint32_t kErrTimeout = 4u;  // a bounded wait gave up
 // block b spans fixed_cost(class) units (what starting it costs a CTA: Q load, epilogue,
 // merge) and then one unit per key tile; the class's U units are cut into C equal ranges
 // [floor(c U / C), floor((c + 1) U / C)), one per persistent CTA.
-__host__ __device__ constexpr int fixed_cost(int cls) { return cls == 0 ? 5 : 2; }
+__host__ __device__ constexpr int fixed_cost(int cls) { return cls == 0 ? 6 : 2; }
 // CTAs a class's U units are cut across: one range per CTA, but no range shorter than
 // kMinRangeUnits (a piece that small costs more in its partial store and merge than it
 // saves: a small problem runs on fewer CTAs, in fewer pieces). Measured on GB300 over 1-6,

@@ -82,8 +82,10 @@ __device__ int blocks_per_head(const SeqInfo& si, int G, int cls) {
 constexpr int kSeqCache = 2048;
 constexpr int kBlockCache = 12288;
 constexpr int kMaxCtas = 1024;
-// fixed_cost(cls) (common.cuh), what starting a row block costs a CTA in key tiles: measured
-// about 8 us at ~1.6 us per tile for verify blocks; prefill blocks have longer tiles.
+// fixed_cost(cls) (common.cuh), what starting a row block costs a CTA in key tiles: per-CTA
+// timestamps on the MTP verify batch put an item beyond a CTA's first at ~9 us, ~6.5 of its
+// 1.42 us tiles; 6 ended the slowest CTA ~1 us earlier than 5 (8 no better); prefill blocks
+// have longer tiles.
 constexpr size_t kPlanSmem = sizeof(int4) * kSeqCache + sizeof(int) * (kSeqCache + 1) +
                              sizeof(long long) * kBlockCache + sizeof(int) * kBlockCache +
                              sizeof(int) * (kMaxCtas + 1);
