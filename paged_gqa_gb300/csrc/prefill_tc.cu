@@ -13,10 +13,13 @@
 //     is one tcgen05.mma kind::f8f6f4 M=128 x N=128 keys x K=256 per tile (8 MMAs of
 //     K=32; bf16 Q is split once per block into e4m3 hi + lo and costs 16);
 //   * P = 2^(s - m + 4) is split into e4m3 hi + lo (about bf16 precision; a single e4m3 P
-//     misses the 5e-3 relative-L2 bar), written into TMEM over the tile's S and used from
-//     there as the A operand of O += P V: M=128 x N=256 (all of d, V as an MN-major operand
-//     whose two 128-byte d-halves sit 16 KB apart), fp32 accumulators in TMEM (O: 256
-//     columns, S: 2 x 128);
+//     misses the 5e-3 relative-L2 bar), written into one of two P buffers in TMEM and used
+//     from there as the A operand of O += P V: M=128 x N=256 (all of d, V as an MN-major
+//     operand whose two 128-byte d-halves sit 16 KB apart), fp32 accumulators in TMEM (S:
+//     128 columns, P: 2 x 64, O: 256). S(g+1) only waits for the softmax to have loaded
+//     S(g), and P(g) for P.V(g-2), so the tensor pipe runs S(g+1) and P.V(g) while the
+//     softmax works on tile g; with P written over its own S, S(g+2) had to wait for
+//     P.V(g), a chain of ~2.4 us per two tiles against ~2 us of tensor work;
 //   * online softmax with one row per TMEM lane: two threads share a row (64 keys each)
 //     and exchange their partial maxima; a row's reference only moves, and its O row is only
 //     rescaled, when a score exceeds the reference by 2^4;
@@ -61,11 +64,12 @@ constexpr uint32_t kQHalf = kRows * 128;        // [128 rows][128 B]
 constexpr uint32_t kQPart = 2 * kQHalf;         // 32 KB
 constexpr uint32_t kKVHalf = kTileKeys * 128;   // [128 keys][128 B]
 constexpr uint32_t kKVTile = 2 * kKVHalf;       // 32 KB
-// TMEM columns: S double buffer (2 x 128), O d-half 0 and 1 (2 x 128). P of a tile replaces
-// the first 64 columns of its S buffer (P_hi 32, P_lo 32: four e4m3 keys per column) and
-// is the A operand of O += P V straight from TMEM.
+// TMEM columns: S (128), two P buffers (2 x 64: P_hi 32 and P_lo 32, four e4m3 keys per
+// column; the A operand of O += P V straight from TMEM), O d-half 0 and 1 (2 x 128).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
+constexpr uint32_t kColP = 128;
+constexpr uint32_t kPBufCols = 64;
 constexpr uint32_t kColO = 256;
 constexpr uint32_t kPCols = kTileKeys / 4;  // 32 columns per P part
 
@@ -89,8 +93,8 @@ struct Misc {
   alignas(16) int lim[2][kRows];
   alignas(16) float merge_w[kMergeMaxSplits * kSlotRows];
   alignas(8) uint64_t k_full[kKStages], k_empty[kKStages], v_full[3], v_empty[3];
-  uint64_t s_full[2], pv_done[2];
-  uint64_t p_full, q_full, q_free, o_ready, o_free, drain[2];
+  uint64_t s_full, s_free, pv_done[2];
+  uint64_t p_full[2], q_full, q_free, o_ready, o_free, drain[2];
   uint64_t never;  // no thread ever arrives (the failure-path test waits on it)
   float qscale[2];
   float amax[kSoftWarps];
@@ -171,10 +175,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       mbar_init(bar(ms.v_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(ms.s_full[b]), 1);
       mbar_init(bar(ms.pv_done[b]), 1);
     }
-    mbar_init(bar(ms.p_full), kSoftThreads);
+    mbar_init(bar(ms.s_full), 1);
+    mbar_init(bar(ms.s_free), kSoftThreads);
+    mbar_init(bar(ms.p_full[0]), kSoftThreads);
+    mbar_init(bar(ms.p_full[1]), kSoftThreads);
     mbar_init(bar(ms.q_full), kSoftThreads);
     mbar_init(bar(ms.q_free), 1);
     mbar_init(bar(ms.o_ready), 1);
@@ -269,8 +275,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   } else if (warp == 1 || warp == kPVIssuerWarp) {
     // ------------------------------------------------------------ MMA issuers
     // One thread cannot issue tcgen05.mma faster than about one per 44 ns, below the tensor
-    // pipe's rate, so S = Q K^T and O += P V come from two warps. P of tile g lives in S
-    // buffer g & 1, so S(g) waits for P.V(g-2); P.V(g) waits for P(g) and V(g).
+    // pipe's rate, so S = Q K^T and O += P V come from two warps. S(g) waits for the softmax
+    // to have loaded S(g-1); P.V(g) waits for P(g) and V(g).
     if (lane == 0) {
       const bool is_s = warp == 1;
       uint32_t g = 0;
@@ -284,7 +290,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             if (j == 0 && !(ok = mbar_wait(bar(ms.q_full), ii & 1, abort_flag, ptr.err))) break;
             const uint32_t st = g % kKStages;
             if (!(ok = mbar_wait(bar(ms.k_full[st]), (g / kKStages) & 1, abort_flag, ptr.err))) break;
-            if (g >= 2 && !(ok = mbar_wait(bar(ms.pv_done[b]), ((g >> 1) - 1) & 1, abort_flag, ptr.err))) break;
+            if (g >= 1 && !(ok = mbar_wait(bar(ms.s_free), (g - 1) & 1, abort_flag, ptr.err))) break;
             tc_fence_after();
             const uint64_t k0 = smem_desc(sbase + LY::kOffK + st * kKVTile, 16, 1024, kSw128);
 #pragma unroll
@@ -293,22 +299,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 #pragma unroll
               for (int kb = 0; kb < 8; ++kb) {
                 const uint32_t qoff = (kb >> 2) * kQHalf + (kb & 3) * 32, koff = (kb >> 2) * kKVHalf + (kb & 3) * 32;
-                mma_e4m3(tmem + kColS + b * 128, q0 + (qoff >> 4), k0 + (koff >> 4), kIdescS, (part | kb) ? 1u : 0u);
+                mma_e4m3(tmem + kColS, q0 + (qoff >> 4), k0 + (koff >> 4), kIdescS, (part | kb) ? 1u : 0u);
               }
             }
-            mma_commit(bar(ms.s_full[b]));
+            mma_commit(bar(ms.s_full));
             mma_commit(bar(ms.k_empty[st]));
             if (j == I.ntiles - 1) mma_commit(bar(ms.q_free));
           } else {
             // the first P.V of an item overwrites O: the previous epilogue must be done
             if (j == 0 && ii >= 1 && !(ok = mbar_wait(bar(ms.o_free), (ii - 1) & 1, abort_flag, ptr.err))) break;
-            if (!(ok = mbar_wait(bar(ms.p_full), g & 1, abort_flag, ptr.err))) break;
+            // one barrier per P buffer: P(g + 2) waits for P.V(g), so the softmax is never two
+            // publications ahead of this wait
+            if (!(ok = mbar_wait(bar(ms.p_full[b]), (g >> 1) & 1, abort_flag, ptr.err))) break;
             const uint32_t st = g % kVStages;
             if (!(ok = mbar_wait(bar(ms.v_full[st]), (g / kVStages) & 1, abort_flag, ptr.err))) break;
             tc_fence_after();
             // V as one N = 256 MN-major operand: d-half 1 is the second 128-byte atom, 16 KB on
             const uint64_t v0 = smem_desc(sbase + LY::kOffV + st * kKVTile, kKVHalf, 1024, kSw128);
-            const uint32_t p_cols = tmem + kColS + b * 128;  // P of this tile, in its S buffer
+            const uint32_t p_cols = tmem + kColP + b * kPBufCols;  // P of this tile
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
 #pragma unroll
@@ -483,16 +491,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         const int key0 = (tile_begin + j) * kTileKeys;
         const int kbase = key0 + kh * kHalfKeys;
         float t[kHalfKeys];
-        if (!mbar_wait(bar(ms.s_full[b]), (g >> 1) & 1, abort_flag, ptr.err)) bad = true;
+        if (!mbar_wait(bar(ms.s_full), g & 1, abort_flag, ptr.err)) bad = true;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < kHalfKeys; k += 16) {
           float v[16];
-          tmem_ld16(tmem + lane_addr + kColS + b * 128 + kh * kHalfKeys + k, v);
+          tmem_ld16(tmem + lane_addr + kColS + kh * kHalfKeys + k, v);
 #pragma unroll
           for (int i = 0; i < 16; ++i) t[k + i] = v[i];
         }
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(ms.s_free));  // S(g+1) may overwrite S now
         // masked tiles hold scaled scores; unmasked tiles keep raw scores and take the
         // scale in the exponent's FFMA
         const bool need_mask = (key0 + kTileKeys > kv_hi) || (key0 + kTileKeys - 1 > min_lim);
@@ -572,19 +582,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             for (int i = 0; i < 8; ++i) dst[i] = z;
           }
         }
-        // P into TMEM over this tile's S: row `row`, keys 64*kh .. 64*kh+63 -> columns
-        // 16*kh .. 16*kh+15 of P_hi (S columns 0..31) and P_lo (S columns 32..63)
-        tmem_st16u(tmem + lane_addr + kColS + b * 128 + kh * 16, ph);
-        tmem_st16u(tmem + lane_addr + kColS + b * 128 + kPCols + kh * 16, pl);
+        // P into P buffer b: row `row`, keys 64*kh .. 64*kh+63 -> columns 16*kh .. 16*kh+15 of
+        // P_hi (buffer columns 0..31) and P_lo (32..63), once P.V(g-2) has read the buffer.
+        // Each tile waits on pv_done[b] once, in order, and P.V(g) needs P(g): the barrier is
+        // never a phase ahead of or two phases behind the one waited for.
+        if (g >= 2 && !mbar_wait(bar(ms.pv_done[b]), ((g >> 1) - 1) & 1, abort_flag, ptr.err)) bad = true;
+        tc_fence_after();
+        tmem_st16u(tmem + lane_addr + kColP + b * kPBufCols + kh * 16, ph);
+        tmem_st16u(tmem + lane_addr + kColP + b * kPBufCols + kPCols + kh * 16, pl);
         tmem_wait_st();
         fence_proxy_async_smem();  // zeroed V rows, if any
         tc_fence_before();
-        mbar_arrive(bar(ms.p_full));
-        // P.V(g-1) has a barrier of its own (its S buffer's), whose next phase needs P(g+1):
-        // the wait cannot mistake a later phase for this one, however late it runs.
-        if (!warp_rescale && g >= 1 &&
-            !mbar_wait(bar(ms.pv_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, abort_flag, ptr.err))
-          bad = true;
+        mbar_arrive(bar(ms.p_full[b]));
       }
       if (it + 1 < item_end) q_prep(load_item(cp, ptr, it + 1), ii + 1);
 
