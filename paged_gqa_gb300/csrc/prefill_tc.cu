@@ -570,9 +570,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           }
           tmem_wait_st();
         }
+        // P.V(g-2) has read P buffer b (and every earlier P.V has completed, so V(g - 2) and
+        // before have landed). Each tile waits on pv_done[b] once, in order, and P.V(g) needs
+        // P(g): the barrier is never a phase ahead of or two phases behind the one waited for.
+        if (g >= 2 && !mbar_wait(bar(ms.pv_done[b]), ((g >> 1) - 1) & 1, abort_flag, ptr.err)) bad = true;
+        tc_fence_after();
         if (key0 + kTileKeys > kv_hi) {
           // keys past the piece's end: their V rows (stale or NaN slots) become zeros.
-          // thread (kh, row) zeroes d-half kh of key `row`
+          // thread (kh, row) zeroes d-half kh of key `row`. This wait skips the phases of
+          // tiles without a tail, so it must not lag two phases: V(g - kVStages) has landed
+          // (P.V(g - 2) above has completed), and V(g + kVStages) cannot land before P.V(g).
           const uint32_t st = g % kVStages;
           if (!mbar_wait(bar(ms.v_full[st]), (g / kVStages) & 1, abort_flag, ptr.err)) bad = true;
           if (key0 + row >= kv_hi) {
@@ -583,11 +590,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           }
         }
         // P into P buffer b: row `row`, keys 64*kh .. 64*kh+63 -> columns 16*kh .. 16*kh+15 of
-        // P_hi (buffer columns 0..31) and P_lo (32..63), once P.V(g-2) has read the buffer.
-        // Each tile waits on pv_done[b] once, in order, and P.V(g) needs P(g): the barrier is
-        // never a phase ahead of or two phases behind the one waited for.
-        if (g >= 2 && !mbar_wait(bar(ms.pv_done[b]), ((g >> 1) - 1) & 1, abort_flag, ptr.err)) bad = true;
-        tc_fence_after();
+        // P_hi (buffer columns 0..31) and P_lo (32..63)
         tmem_st16u(tmem + lane_addr + kColP + b * kPBufCols + kh * 16, ph);
         tmem_st16u(tmem + lane_addr + kColP + b * kPBufCols + kPCols + kh * 16, pl);
         tmem_wait_st();
