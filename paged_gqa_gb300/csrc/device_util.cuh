@@ -131,6 +131,9 @@ __device__ __forceinline__ bool split_arrive(unsigned long long* counter, int ns
 // ("Optimize Qwen3.5 MTP unified attention on gfx950": split-KV segments reduced by
 // a second pass). s_w is shared scratch of kMergeMaxSplits * kSlotRows floats.
 // Returns after the merge (if any) is complete.
+__device__ inline void merge_split_block(const Problem& p, const Pointers& ptr, const ClassPlan& cp,
+                                         const RowBlock& rb, int tid, int nthreads, int bar_id, float* s_w);
+
 __device__ inline void finish_split_block(const Problem& p, const Pointers& ptr, const ClassPlan& cp,
                                           int block_index, const RowBlock& rb, int tid, int nthreads,
                                           int bar_id, int* s_flag, float* s_w) {
@@ -141,7 +144,13 @@ __device__ inline void finish_split_block(const Problem& p, const Pointers& ptr,
     __threadfence();
   }
   named_barrier(bar_id, nthreads);
-  if (!*s_flag) return;
+  if (*s_flag) merge_split_block(p, ptr, cp, rb, tid, nthreads, bar_id, s_w);
+}
+
+// The merge of finish_split_block, for a caller that has arrived itself (its arriving thread
+// fenced after the atomic and the callers passed a barrier since) and is the block's last.
+__device__ inline void merge_split_block(const Problem& p, const Pointers& ptr, const ClassPlan& cp,
+                                         const RowBlock& rb, int tid, int nthreads, int bar_id, float* s_w) {
   __threadfence();
   const int seq_q0 = ptr.qsl[rb.seq];
   const int ns = rb.nsplit;

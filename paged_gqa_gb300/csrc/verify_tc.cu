@@ -649,20 +649,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         fence_proxy_async_smem();
         named_barrier(1, kSoftThreads);
         if (gi == 0) {
-          const bool last_item = it + 1 == item_end && I.nsplit <= kMergeMaxSplits;
           // the counter's current word travels while the partial is written
-          const unsigned long long seen = last_item ? split_peek(cp.counters + I.block) : 0ull;
+          const unsigned long long seen = split_peek(cp.counters + I.block);
           bulk_store(slot_o(cp, slot), smem_u32(stage), (uint32_t)I.nrows * kHeadDim * 2u);
           bulk_store(slot_lse(cp, slot), smem_u32(ms.lse_stage), kVN * 4u);  // all 64 entries of the slot
           bulk_commit();
           bulk_wait_all();  // the partial is in global memory before the split counter moves
           fence_proxy_async_global();
-          if (last_item) {
-            // the CTA's last item: is this piece the block's last? (merged below)
-            __threadfence();
-            ms.merge_flag = split_arrive_from(cp.counters + I.block, seen, I.nsplit, split_tag(p, cp));
-            __threadfence();
-          }
+          // is this piece the block's last? (merged below)
+          __threadfence();
+          ms.merge_flag = split_arrive_from(cp.counters + I.block, seen, I.nsplit, split_tag(p, cp));
+          __threadfence();
         }
         named_barrier(1, kSoftThreads);  // the stage is reused by the next item's P; merge_flag
       } else {
@@ -757,7 +754,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
               named_barrier(2, kSoftThreads);  // the buffers are reused by the next pass
             }
           }
-        } else {
+        } else if (ms.merge_flag) {
+          // a piece that is not its CTA's last item (or one of more than kMergeMaxSplits) and
+          // arrived last: merge from global memory
           RowBlock rb;
           rb.seq = I.seq;
           rb.kvh = I.kvh;
@@ -765,7 +764,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           rb.nrows = I.nrows;
           rb.nsplit = I.nsplit;
           rb.slot_base = I.slot_base;
-          finish_split_block(p, ptr, cp, I.block, rb, gi, kSoftThreads, 2, &ms.merge_flag, ms.merge_w);
+          merge_split_block(p, ptr, cp, rb, gi, kSoftThreads, 2, ms.merge_w);
         }
       }
 #pragma unroll
