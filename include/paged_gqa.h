@@ -139,9 +139,9 @@ int paged_gqa_attn_ex(const pg_tensor* q, const pg_tensor* k_cache, const pg_ten
  * uses a 64 MiB scratch array that is part of the library's device image: every GPU that
  * loads the library holds those 64 MiB until the process exits. It allocates nothing.
  * A call whose workspace need (paged_gqa_workspace_size) exceeds 64 MiB returns
- * PG_ERR_WORKSPACE and launches nothing. All calls on a device share the array; each
- * call clears what must start at zero, but calls that can overlap on the GPU (unordered
- * streams) race on it. The first call on each device looks up the array's address with
+ * PG_ERR_WORKSPACE and launches nothing. All calls on a device share the array; nothing
+ * in it needs clearing (the split counters carry a per-call tag), but calls that can
+ * overlap on the GPU (unordered streams) race on it. The first call on each device looks up the array's address with
  * that device current: make it before any stream capture.
  */
 int paged_gqa_attn_noalloc(const pg_tensor* q, const pg_tensor* k_cache, const pg_tensor* v_cache,
