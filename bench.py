@@ -265,6 +265,41 @@ def attn_spec(args) -> wl.CaseSpec:
     return spec
 
 
+def _time_graph(pg, case, out, flush, K, warmup):
+    """The caller-workspace call (paged_gqa_attn_ex) captured once in a CUDA graph, then
+    replayed K times with the same L2 flush before each replay (outside the events): the
+    call's cost without its host-side launch work. Returns the median us per replay."""
+    spec = case.spec
+    ws = torch.empty(pg.paged_gqa_workspace_size(spec.num_seqs, spec.total_q, spec.num_q_heads, spec.num_kv_heads,
+                                                 spec.page_size, case.block_table.shape[1],
+                                                 torch.cuda.current_device()),
+                     dtype=torch.uint8, device=out.device)
+
+    def call_ex():
+        pg.paged_gqa_attn_ex(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                             case.query_start_loc, 1.0, case.k_descale, case.v_descale, case.softmax_scale, out, ws)
+
+    call_ex()  # per-device set-up happens outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call_ex()
+    for _ in range(max(3, warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert pg.paged_gqa_check_device_errors() == 0, pg.paged_gqa_last_error()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record()
+        graph.replay()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
+    del graph, ws
+    return us
+
+
 def _time_attn(pg, call, flush, K, warmup, dominant_cls, local, world):
     """Per-call CUDA events over K calls (an L2 flush before each, outside the events),
     then a second pass with the library's events around the dominant kernel. Returns
@@ -379,6 +414,9 @@ def extra_config(pg, args, idx, dev, flush, local, world, quant_q):
          "roofline": _roofline(spec, kind, sum(kern_ms) / K, _kernel_kind(plan, cls, kind, spec), clocks,
                                q_split=spec.q_dtype == "bf16" and not quant_q),
          "path_bits": int(plan["path_bits"]), "clocks": clocks, "kv_bytes": spec.kv_bytes, "flops": spec.flops}
+    if idx == 1 and not quant_q:
+        # the launch-bound tiny call: also as one CUDA-graph replay
+        r["graph_us_per_call"] = round(_time_graph(pg, case, out, flush, K, args.warmup), 2)
     if not args.no_cpu_baseline:
         r["cpu_baseline"] = cpu_baseline(spec, case, args.extra_cpu_seconds, kind, quant_q)
     del case, out
@@ -440,10 +478,12 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         e2e_ms = statistics.median(a.elapsed_time(b) for a, b in e_ev)
         e2e = (e2e_ms, h2d, d2h)
+    # the same call as one CUDA-graph replay (no host launch work)
+    graph_us = _time_graph(pg, case, out, flush, K, args.warmup) if args.op == "attn" else 0.0
 
     # reduce over ranks: max time
-    step_ms, step_mean_ms, kern_avg_ms, e2e_ms = max_over_ranks(
-        [step_ms, step_mean_ms, kern_avg_ms, e2e[0] if e2e else 0.0], world, dev)
+    step_ms, step_mean_ms, kern_avg_ms, e2e_ms, graph_us = max_over_ranks(
+        [step_ms, step_mean_ms, kern_avg_ms, e2e[0] if e2e else 0.0, graph_us], world, dev)
     if rank != 0:
         return None
     cpu = None
@@ -474,6 +514,8 @@ def run_ours(args, rank, world, local):
         "wall_s": round(wall, 3),
         "stat": "value and ms_per_step from the median call; roofline.achieved from the mean kernel time",
     }
+    if graph_us > 0:
+        res["graph_us_per_call"] = round(graph_us, 2)
     if e2e:
         res["e2e"] = {"value": round(per_step * world / (e2e_ms / 1e3), 3), "unit": unit,
                       "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2],
