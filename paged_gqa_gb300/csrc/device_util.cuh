@@ -100,6 +100,12 @@ __device__ __forceinline__ unsigned long long split_tag(const Problem& p, const 
   return (__ldcg(cp.epoch) ^ ((unsigned long long)p.call_tag * 0x9E3779B97F4A7C15ull)) & kSplitTagMask;
 }
 
+// Acquire-release fence at GPU scope: around a relaxed atomic, it makes the atomic a release
+// of this thread's earlier writes (for the pieces that arrive at a split counter) and an
+// acquire of the other pieces' partials (for the last one). A plain message-passing pattern,
+// so no sequentially consistent fence is needed.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // One piece of a split block has stored its partial; true for the block's last piece. The
 // counter word holds (tag << 16) | arrivals (nsplit < 2^16); a word with another tag counts
 // as no arrivals. The CAS loop retries only while other pieces of the block arrive.

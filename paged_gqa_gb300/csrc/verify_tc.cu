@@ -300,6 +300,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     // and every producer drains the copies it issued.
     const bool stalled = p.stall_test_ns && !mbar_wait(bar(ms.never), 0, abort_flag, ptr.err, p.stall_test_ns);
     if (!stalled) {
+    // This call's split-counter tag, read once: the epoch word does not move while this grid
+    // runs (the plan kernel advances it after this grid, or before it and before the wait
+    // above), and the load's latency then stays off every arrival.
+    const unsigned long long ctag = gi == 0 ? split_tag(p, cp) : 0ull;
 
     auto q_prep = [&](const Item& I, int ii) {
       const int pi = ii & 1;
@@ -657,9 +661,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           bulk_wait_all();  // the partial is in global memory before the split counter moves
           fence_proxy_async_global();
           // is this piece the block's last? (merged below)
-          __threadfence();
-          ms.merge_flag = split_arrive_from(cp.counters + I.block, seen, I.nsplit, split_tag(p, cp));
-          __threadfence();
+          fence_acq_rel_gpu();
+          ms.merge_flag = split_arrive_from(cp.counters + I.block, seen, I.nsplit, ctag);
+          fence_acq_rel_gpu();
         }
         named_barrier(1, kSoftThreads);  // the stage is reused by the next item's P; merge_flag
       } else {
