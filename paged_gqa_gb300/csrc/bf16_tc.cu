@@ -439,12 +439,9 @@ bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant
         tmem_wait_ld();
         // scaled scores, masked past the row's causal limit and the piece's end
         const bool need_mask = (key0 + kSub > kv_hi) || (key0 + kSub - 1 > min_lim);
-        float mx = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < kHalfKeys; ++i) {
-          t[i] = (!need_mask || kbase + i <= hi_key) ? t[i] * c : -INFINITY;
-          mx = fmaxf(mx, t[i]);
-        }
+        for (int i = 0; i < kHalfKeys; ++i) t[i] = (!need_mask || kbase + i <= hi_key) ? t[i] * c : -INFINITY;
+        const float mx = extreme_of<true>(t);
         // the row's maximum over both key halves (partner: same lane, the other warp)
         ms.red[g & 1][kh][row] = mx;
         named_barrier(pair_bar, 64);

@@ -506,21 +506,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         // masked tiles hold scaled scores; unmasked tiles keep raw scores and take the
         // scale in the exponent's FFMA
         const bool need_mask = (key0 + kTileKeys > kv_hi) || (key0 + kTileKeys - 1 > min_lim);
-        float mx = -INFINITY;
+        float mx;
         if (need_mask) {
 #pragma unroll
-          for (int i = 0; i < kHalfKeys; ++i) {
-            t[i] = (kbase + i <= hi_key) ? t[i] * c : -INFINITY;
-            mx = fmaxf(mx, t[i]);
-          }
-        } else if (c_pos) {
-#pragma unroll
-          for (int i = 0; i < kHalfKeys; ++i) mx = fmaxf(mx, t[i]);
-          mx *= c;
+          for (int i = 0; i < kHalfKeys; ++i) t[i] = (kbase + i <= hi_key) ? t[i] * c : -INFINITY;
+          mx = extreme_of<true>(t);
         } else {
-#pragma unroll
-          for (int i = 0; i < kHalfKeys; ++i) mx = fmaxf(mx, -t[i]);
-          mx *= -c;
+          // max of s c = c max(s) for c >= 0, c min(s) for c < 0
+          mx = (c_pos ? extreme_of<true>(t) : extreme_of<false>(t)) * c;
         }
         // the row's maximum over both key halves (partner: same lane, the other warp)
         ms.red[g & 1][kh][row] = mx;

@@ -285,6 +285,38 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// The largest / smallest of three (max.f32 / min.f32 with three inputs, sm_100 and later):
+// one instruction where two-input ones take two dependent steps. Same NaN rule as fmaxf.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// Maximum (kMax) or minimum of N values: four independent chains of N / 4 values each, of
+// three-input steps, then their combination. 34 instructions, 10 deep, for N = 64, against
+// 63 dependent ones for a plain running maximum; the result is the same value.
+template <bool kMax, int N>
+__device__ __forceinline__ float extreme_of(const float (&t)[N]) {
+  static_assert(N % 8 == 0, "four chains of an even number of values");
+  constexpr int kQ = N / 4;
+  auto f3 = [](float a, float b, float c) { return kMax ? max3f(a, b, c) : min3f(a, b, c); };
+  auto f2 = [](float a, float b) { return kMax ? fmaxf(a, b) : fminf(a, b); };
+  float a[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) a[k] = t[k * kQ];
+#pragma unroll
+  for (int i = 1; i + 1 < kQ; i += 2)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) a[k] = f3(a[k], t[k * kQ + i], t[k * kQ + i + 1]);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) a[k] = f2(a[k], t[k * kQ + kQ - 1]);
+  return f3(f2(a[0], a[1]), a[2], a[3]);
+}
 __device__ __forceinline__ float warp_max(float v) {
   float r;
   asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
