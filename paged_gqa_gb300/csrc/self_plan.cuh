@@ -34,10 +34,11 @@ __device__ __forceinline__ int cut_cta(const Cut& k, int u) {
   return c;
 }
 
-// Scratch of the prologue (12 KB), in shared memory no copy has touched yet.
+// Scratch of the prologue (20 KB), in shared memory no copy has touched yet.
 struct Scratch {
   long long v[kFusedMaxBlocks];  // per sequence: (units << 16) | 1 for a verify sequence, else 0
   int tiles[kFusedMaxBlocks];    // per sequence: key tiles of each of its blocks
+  int4 seq[kFusedMaxBlocks];     // per sequence: {first token, q_len, L, 0} as read
   int fv_seq[kFusedMaxBlocks];   // per verify sequence j: its index,
   int fv_off[kFusedMaxBlocks];   // the first unit of its blocks,
   int fv_tiles[kFusedMaxBlocks]; // its tiles per block
@@ -58,16 +59,18 @@ __device__ __forceinline__ void load(const Problem& p, const Pointers& ptr, Scra
     }
     fs.v[s] = v;
     fs.tiles[s] = tiles;
+    fs.seq[s] = make_int4(q0, qn, L, 0);
   }
 }
 
 // Step 2, one warp, after a CTA barrier: the scan over sequences (each lane a contiguous
 // run of them), this CTA's range and items. Packed item (fitem, at most kFusedMaxBlocks):
 // x = block, y = sequence, z = first tile | tiles << 16, w = piece index | pieces << 15 |
-// (1 << 30 if the block's first CTA's range starts in an earlier block). *fcount gets the
-// number of items.
+// (1 << 30 if the block's first CTA's range starts in an earlier block); fseq gets the
+// item's sequence {first token, q_len, L, 0}, so that no item load reads global memory.
+// *fcount gets the number of items.
 __device__ __forceinline__ void plan_warp(const Problem& p, Scratch& fs, int num_ctas, int lane, int4* fitem,
-                                          int* fcount) {
+                                          int4* fseq, int* fcount) {
   const int n = p.num_seqs;
   const int per = (n + 31) / 32;
   const int s0 = lane * per, s1 = min(n, s0 + per);
@@ -123,11 +126,12 @@ __device__ __forceinline__ void plan_warp(const Problem& p, Scratch& fs, int num
     const int nsplit = cut_cta(k, real + tiles - 1) - c0 + 1;
     const int later = cut_begin(k, c0) < off ? 1 : 0;
     fitem[t] = make_int4(b, fs.fv_seq[j], (lo - real) | ((hi - lo) << 16), (c - c0) | (nsplit << 15) | (later << 30));
+    fseq[t] = fs.seq[fs.fv_seq[j]];
   }
   if (lane == 0) *fcount = cnt;
 }
 
-// A packed item, unpacked; the caller adds what it reads from query_start_loc / seq_lens.
+// A packed item, unpacked; the caller adds its sequence's record (fseq).
 struct Piece {
   int block, seq, kvh, tile_begin, ntiles, split, nsplit, slot_base;
 };

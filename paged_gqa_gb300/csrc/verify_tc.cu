@@ -127,6 +127,7 @@ struct Misc {
   // Self-planned verify class (Problem::fused_verify): this CTA's items, packed by
   // self_plan::plan_warp, and their count.
   int4 fitem[kFusedMaxBlocks];
+  int4 fseq[kFusedMaxBlocks];  // each item's sequence: {first token, q_len, L, 0}
   int fcount;
 };
 static_assert(offsetof(Misc, m) % 16 == 0 && offsetof(Misc, k_full) % 8 == 0, "Misc alignment");
@@ -152,9 +153,10 @@ __device__ __forceinline__ Item load_item_fused(const Problem& p, const Pointers
   r.split = f.split;
   r.nsplit = f.nsplit;
   r.slot_base = f.slot_base;
-  r.q0 = ptr.qsl[r.seq];
-  r.qn = ptr.qsl[r.seq + 1] - r.q0;
-  r.L = ptr.seq_lens[r.seq];
+  const int4 sq = ms.fseq[it];
+  r.q0 = sq.x;
+  r.qn = sq.y;
+  r.L = sq.z;
   r.row0 = 0;
   r.nrows = r.qn * p.G;
   r.kv_end = r.L;  // the causal limit of the last row (token qn - 1) is L
@@ -258,7 +260,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   }
   if (kFused) {
     __syncthreads();  // the sequences are staged
-    if (warp == 1) self_plan::plan_warp(p, fs, cp.num_ctas, lane, ms.fitem, &ms.fcount);
+    if (warp == 1) self_plan::plan_warp(p, fs, cp.num_ctas, lane, ms.fitem, ms.fseq, &ms.fcount);
   }
   tc_fence_before();
   __syncthreads();
