@@ -166,6 +166,34 @@ def test_self_planned_verify_at_its_limit(path):
         _assert_tcgen05_only(path, case)
 
 
+@pytest.mark.parametrize("i", range(6))
+def test_self_planned_verify_matches_the_plan_kernel_bit_for_bit(i):
+    """A verify kernel that plans its own class takes exactly the plan kernel's cut: the same
+    pieces on the same CTAs, and merges that add every piece's partial in piece order
+    whichever piece arrives last. So both planning paths give the same output bits, on
+    random MTP batches from 1 to 200 sequences, contexts up to 40k keys (blocks split over
+    many CTAs), one and two kv heads, e4m3 and bf16 caches."""
+    import paged_gqa_gb300 as pg
+    gen = torch.Generator().manual_seed(600 + i)
+    n = [1, 7, 64, 150, 200, 40][i]
+    hkv = [1, 2, 1, 1, 2, 1][i]
+    Ls = torch.randint(1, 40000 if n <= 64 else 12000, (n,), generator=gen).tolist()
+    qs = torch.randint(1, 5, (n,), generator=gen).tolist()
+    spec = wl.CaseSpec(f"self-plan {i}", [(min(q, L), L) for q, L in zip(qs, Ls)], 16 * hkv, hkv, 16,
+                       kv_dtype="bf16" if i == 5 else "e4m3")
+    case = wl.make_case(spec, device="cuda", seed=600 + i, poison=True)
+    outs = []
+    for p in (0, 3):
+        prev = pg.paged_gqa_set_path(p)
+        try:
+            outs.append(gu.run_library(case))
+            assert pg.paged_gqa_last_plan()["verify_self_planned"] == (1 if p == 0 else 0)
+        finally:
+            pg.paged_gqa_set_path(prev)
+    assert torch.isfinite(outs[0].float()).all()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16)), f"case {i}"
+
+
 def test_decode_batch(path):
     """Pure decode: every sequence has one new token (q_len 1), G = 8, two kv heads."""
     gen = torch.Generator().manual_seed(31)
